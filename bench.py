@@ -1,0 +1,455 @@
+#!/usr/bin/env python3
+"""Dispatch + combine benchmark on one GB300.
+
+One step = one MoE layer's hot path over one batch: route_count, exchange,
+dispatch_send, dispatch_recv (dispatch) and combine_send, combine_recv
+(combine), each a launch of libmoeroute through its C ABI.  The grouped-GEMM
+stand-in runs once before timing (its output is the same every step) and is
+not timed.  Inputs are resident in HBM when timing starts; L2 is flushed
+(512 MiB write) before every step, outside the timed window.
+
+Prints one JSON line: value = dispatch + combine microseconds per layer
+(lower is better), plus achieved HBM GB/s over the algorithmic bytes, the
+roofline of the dominant kernel, an end-to-end figure with host buffers, and
+the CPU oracle timed on a bounded sample as a baseline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+  python bench.py --impl reference ...   (the CPU oracle as the reference arm)
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "dispatch+combine µs/layer and achieved HBM GB/s (% of GB300 peak) at EP16 h7168"
+UNIT = "us/layer"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 512 << 20
+KERNELS = ("route_count", "exchange", "dispatch_send", "dispatch_recv", "combine_send",
+           "combine_recv")
+KERNEL_SYMBOL = {"route_count": "k_route_count", "exchange": "k_exchange",
+                 "dispatch_send": "k_quant_pack", "dispatch_recv": "k_row_shuffle<DispatchMap>",
+                 "combine_send": "k_row_shuffle<CombineMap>", "combine_recv": "k_combine_reduce"}
+
+
+# ----------------------------------------------------------------- bytes
+
+
+def algorithmic_bytes(w, A: int) -> dict:
+    """Bytes each step must move, every materialised buffer written once and
+    read once; A = (token, expert) assignments routed.  Row_fp8 = H + 4*Sb."""
+    N, T, H, R = w.N, w.T, w.H, w.R
+    Sb = H // 128
+    row8 = H + 4 * Sb
+    x = 2 * N * T * H
+    per = {
+        "dispatch_send": x + A * (row8 + 4) + 4 * A,           # read x, slots; write rows+tok
+        "dispatch_recv": A * (row8 + 4) + A * (row8 + 8),      # read rows+tok; write rows+src
+        "combine_send": 2 * A * 2 * H,                          # read y rows; write csend rows
+        "combine_recv": A * 2 * H + x + 12 * A,                 # read rows, idx/w/slot; write out
+    }
+    dispatch = x + 3 * A * row8 + 8 * A
+    combine = 3 * A * 2 * H + x + 8 * A
+    return {"per_kernel": per, "dispatch": dispatch, "combine": combine,
+            "total": dispatch + combine}
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "combine_expert_count_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def dram_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu capture, or None when absent
+    or taken on a different kernel source."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    try:
+        lines = open(p).read().splitlines()
+    except OSError:
+        return None
+    src = _source_hash()
+    for ln in lines:
+        parts = ln.split()
+        if len(parts) >= 4 and not ln.startswith("#") and parts[0] == kernel and \
+                parts[1] == workload and parts[3] == src:
+            return int(parts[2])
+    return None
+
+
+# ----------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.idx = gpu_id
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return None
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for ln in f:
+                p = [x.strip() for x in ln.split(",")]
+                if len(p) >= 9:
+                    rows.append(p)
+        os.unlink(self.file.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def gpu_id(local: int) -> str:
+    """nvidia-smi -i argument for this process's GPU (its UUID when torch
+    exposes it, so CUDA_VISIBLE_DEVICES remapping does not matter)."""
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(local).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except (AttributeError, RuntimeError):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [v for v in vis.split(",") if v.strip()]
+        return ids[local] if local < len(ids) else str(local)
+
+
+# ----------------------------------------------------------------- dist
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------- CPU oracle
+
+
+def oracle_layer_us(w, sample_T: int, min_seconds: float, max_reps: int = 10):
+    """The CPU oracle, as it stands, on a sample of the workload (sample_T of
+    the T tokens per rank, all ranks); microseconds per full layer, scaled by
+    T / sample_T (every step is linear in the number of tokens)."""
+    from combine_expert_count_gb300 import workloads as W
+    from oracle import ref
+    ws = w.replace(T=sample_T, seed=w.seed + 17)
+    d = W.generate(ws)
+    mode = 1 if w.expert == "scale" else 0
+    times = []
+    t_start = time.perf_counter()
+    while len(times) < max_reps:
+        t0 = time.perf_counter()
+        rc = ref.route_count(ws.N, ws.T, ws.E, ws.R, d["topk_idx"])
+        ex = ref.exchange(ws.N, ws.E, 1 << 30, rc["expert_count"], rc["send_off"])
+        cap = max(1, int(ex["grp_off"][:, -1].max()))
+        ref.layer(ws.N, ws.T, ws.E, ws.R, ws.H, cap, d["x"], d["topk_idx"], d["topk_w"], mode)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_start >= min_seconds:
+            break
+    per_layer = statistics.median(times) * (w.T / sample_T) * 1e6
+    sample = (f"{ws.N} ranks x {sample_T} of {w.T} tokens/rank (H={w.H}, E={w.E}, top-{w.R}), "
+              f"{len(times)} runs, median, scaled x{w.T / sample_T:g}")
+    return per_layer, sample, sum(times)
+
+
+# ----------------------------------------------------------------- arms
+
+
+def run_reference(args) -> None:
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from combine_expert_count_gb300 import workloads as W
+    from oracle import ref
+    ref.build()
+    w = W.CONFIGS[args.config]
+    sample_T = max(1, min(w.T, args.ref_tokens))
+    for _ in range(args.warmup):
+        oracle_layer_us(w, sample_T, 0.0, max_reps=1)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        v, sample, _ = oracle_layer_us(w, sample_T, 0.0, max_reps=1)
+        vals.append(v)
+    wall = time.perf_counter() - t0
+    value = statistics.mean(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(value / 1000, 4), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8/f32 (plain C, fp32 accumulation)",
+        "data": "synthetic (seeded)",
+        "config": {"workload": args.config, "N": w.N, "T": w.T, "H": w.H, "E": w.E, "R": w.R},
+        "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "wall_s": round(wall, 1),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args) -> None:
+    import torch
+
+    from combine_expert_count_gb300 import moeroute as m
+    from combine_expert_count_gb300 import workloads as W
+
+    world, rank, local = dist_setup()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    m.lib()  # raises if the library is not built
+
+    w = W.CONFIGS[args.config]
+    d = W.generate(w)
+    buf = m.MoeBuffers(w.N, w.T, w.E, w.R, w.H, device=dev)
+    x = torch.from_numpy(d["x"].view(np.int16)).to(dev)
+    idx = torch.from_numpy(d["topk_idx"]).to(dev)
+    wt = torch.from_numpy(d["topk_w"]).to(dev)
+    sh = buf.shape
+    mode = 1 if w.expert == "scale" else 0
+
+    # one untimed pass, and the expert stand-in whose output every step reuses
+    buf.dispatch(x, idx)
+    buf.expert(mode)
+    buf.combine(idx, wt)
+    torch.cuda.synchronize()
+    status = int(buf.status.item())
+    if status != 0:
+        raise RuntimeError(f"device status {status}: {m.strerror(status)}")
+    A = int(buf.send_off[:, -1].sum().item())
+    nbytes = algorithmic_bytes(w, A)
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        calls = (
+            lambda: m.moe_route_count(sh, idx, buf.expert_count, buf.send_off,
+                                      buf.expert_send_off, buf.slot_row, buf.status),
+            lambda: m.moe_exchange(sh, buf.expert_count, buf.send_off, buf.grp_off, buf.seg_off,
+                                   buf.csend_off, buf.m_sizes, buf.status),
+            lambda: m.moe_dispatch_send(sh, x, buf.slot_row, buf.send_q, buf.send_s,
+                                        buf.send_tok, buf.status),
+            lambda: m.moe_dispatch_recv(sh, buf.send_q, buf.send_s, buf.send_tok,
+                                        buf.expert_count, buf.expert_send_off, buf.seg_off,
+                                        buf.grp_q, buf.grp_s, buf.grp_src, buf.status),
+            lambda: m.moe_combine_send(sh, buf.y, buf.expert_count, buf.expert_send_off,
+                                       buf.send_off, buf.seg_off, buf.csend_off, buf.csend,
+                                       buf.status),
+            lambda: m.moe_combine_recv(sh, buf.csend, idx, wt, buf.slot_row, buf.send_off,
+                                       buf.csend_off, buf.out, buf.status),
+        )
+        for i, c in enumerate(calls):
+            c()
+            if ev is not None:
+                ev[i + 1].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(KERNELS) + 1)]
+           for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_id(local)) as clk:
+        t_wall = time.perf_counter()
+        for k in range(K):
+            flush.zero_()
+            evs[k][0].record(stream)
+            step(evs[k])
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    barrier(world)
+    per_kernel_ms = {name: [] for name in KERNELS}
+    step_ms = []
+    for ev in evs:
+        for i, name in enumerate(KERNELS):
+            per_kernel_ms[name].append(ev[i].elapsed_time(ev[i + 1]))
+        step_ms.append(ev[0].elapsed_time(ev[-1]))
+    mean_step_ms = max_over_ranks(statistics.mean(step_ms), world)
+    disp_ms = statistics.mean(sum(per_kernel_ms[n][k] for n in KERNELS[:4]) for k in range(K))
+    comb_ms = statistics.mean(sum(per_kernel_ms[n][k] for n in KERNELS[4:]) for k in range(K))
+    status = int(buf.status.item())
+
+    # end to end: host buffers in pinned memory, copies inside the timed window
+    xh = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    xh.copy_(x)
+    ih = torch.empty(idx.shape, dtype=idx.dtype, pin_memory=True)
+    ih.copy_(idx)
+    wh = torch.empty(wt.shape, dtype=wt.dtype, pin_memory=True)
+    wh.copy_(wt)
+    oh = torch.empty(buf.out.shape, dtype=buf.out.dtype, pin_memory=True)
+    x2, i2, w2 = torch.empty_like(x), torch.empty_like(idx), torch.empty_like(wt)
+    e2e_ms = []
+    for k in range(K + max(args.warmup, 3)):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        x2.copy_(xh, non_blocking=True)
+        i2.copy_(ih, non_blocking=True)
+        w2.copy_(wh, non_blocking=True)
+        buf.dispatch(x2, i2)
+        buf.combine(i2, w2)
+        oh.copy_(buf.out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if k >= max(args.warmup, 3):
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e_us = max_over_ranks(statistics.mean(e2e_ms), world) * 1000
+    h2d = xh.numel() * xh.element_size() + ih.numel() * 4 + wh.numel() * 4
+    d2h = oh.numel() * oh.element_size()
+
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peak()
+    us = mean_step_ms * 1000
+    achieved = nbytes["total"] / (us * 1e-6) / 1e9
+    # dominant kernel: the largest share of the step
+    avg = {n: statistics.mean(per_kernel_ms[n]) for n in KERNELS}
+    dom = max(("dispatch_send", "dispatch_recv", "combine_send", "combine_recv"), key=avg.get)
+    dom_gbs = nbytes["per_kernel"][dom] / (avg[dom] * 1e-3) / 1e9
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": round(us, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(mean_step_ms, 5),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8-e4m3 dispatch (fp32 scales), bf16 combine with f32 accumulation",
+        "data": "synthetic (seeded N(0,1) activations, softmax top-k routing)",
+        "config": {"workload": f"{args.config}: N={w.N} ranks x T={w.T} tokens, H={w.H}, "
+                               f"E={w.E}, top-{w.R}, cap={buf.cap}, expert stand-in "
+                               f"{'per-expert scale' if mode else 'identity'}",
+                   "N": w.N, "T": w.T, "H": w.H, "E": w.E, "R": w.R, "cap": buf.cap,
+                   "l2": "flushed before every step (512 MiB write, outside the timed window)",
+                   "parallelism": "ranks simulated as slices of one GPU; replicas across GPUs"},
+        "dispatch_us": round(disp_ms * 1000, 2), "combine_us": round(comb_ms * 1000, 2),
+        "achieved_gbs": round(achieved, 1),
+        "frac_of_peak": round(achieved / peak, 4), "peak_gbs": peak, "peak_kind": peak_kind,
+        "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
+        "algorithmic_mb": {"dispatch": round(nbytes["dispatch"] / 1e6, 1),
+                           "combine": round(nbytes["combine"] / 1e6, 1)},
+        "kernel_us": {n: round(avg[n] * 1000, 2) for n in KERNELS},
+        "roofline": {"bound": "hbm", "kernel": KERNEL_SYMBOL[dom],
+                     "achieved": round(dom_gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(dom_gbs / peak, 4),
+                     "traffic": dram_traffic(dom, args.config),
+                     "algorithmic_bytes": nbytes["per_kernel"][dom]},
+        "e2e": {"value": round(e2e_us, 2), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": len(KERNELS) * K,
+        "clocks": clocks,
+        "status": status,
+        "wall_s_timed": round(t_wall, 3),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        v, sample, spent = oracle_layer_us(w, max(1, min(w.T, args.ref_tokens)), args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(v, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": sample, "cpu_seconds": round(spent, 1)}
+    print(json.dumps(line), flush=True)
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="dsv3_decode")
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--ref-tokens", type=int, default=16,
+                    help="tokens per rank in each oracle sample")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="minimum CPU time spent on the oracle baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

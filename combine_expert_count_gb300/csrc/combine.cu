@@ -1,0 +1,194 @@
+// combine.cu -- combine receive (weighted average accumulated on the
+// receiving side), the grouped-GEMM stand-in, and the element-wise e4m3
+// encoder, after "Enabling trillion-parameter models on AWS EFA", section
+// "Dispatch and combine" (combine reads the receive buffer and accumulates
+// each token's weighted average into the output).
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+
+// ------------------------------------------------------------ combine reduce
+//
+// One 128-thread block per token (grid-stride over tokens).  Threads 0..R-1
+// resolve where each of the token's R rows sits (rank p = e/Er, row
+// csend_off[p][s] + slot - send_off[s][p]) into shared memory; then every
+// thread takes 16-byte chunks of the row, issues the R loads, and folds them
+// into fp32 accumulators with one fused multiply-add per slot in slot order
+// k = 0..R-1, rounding once to bf16 at the end.
+constexpr int kReduceThreads = 128;
+constexpr int kReduceGroup = 8;  // row loads kept in flight per chunk
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+    const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+    return l | (h << 16);
+}
+
+__device__ __forceinline__ void fma8(float (&acc)[8], float w, const uint4 &v) {
+    acc[0] = __fmaf_rn(w, bf16_lo(v.x), acc[0]);
+    acc[1] = __fmaf_rn(w, bf16_hi(v.x), acc[1]);
+    acc[2] = __fmaf_rn(w, bf16_lo(v.y), acc[2]);
+    acc[3] = __fmaf_rn(w, bf16_hi(v.y), acc[3]);
+    acc[4] = __fmaf_rn(w, bf16_lo(v.z), acc[4]);
+    acc[5] = __fmaf_rn(w, bf16_hi(v.z), acc[5]);
+    acc[6] = __fmaf_rn(w, bf16_lo(v.w), acc[6]);
+    acc[7] = __fmaf_rn(w, bf16_hi(v.w), acc[7]);
+}
+
+__global__ void __launch_bounds__(kReduceThreads)
+    k_combine_reduce(int N, int T, int E, int R, int H, int cap,
+                     const uint16_t *__restrict__ csend, const int32_t *__restrict__ idx,
+                     const float *__restrict__ w, const int32_t *__restrict__ slot_row,
+                     const int32_t *__restrict__ send_off, const int32_t *__restrict__ csend_off,
+                     uint16_t *__restrict__ out) {
+    __shared__ long long src[MOE_MAX_TOPK];  // element offset of row k in csend, -1: skip
+    __shared__ float wk[MOE_MAX_TOPK];
+    const int Er = E / N, cpr = H >> 3;
+    const long long ntok = (long long)N * T;
+    for (long long tok = blockIdx.x; tok < ntok; tok += gridDim.x) {
+        const int s = (int)(tok / T);
+        if (threadIdx.x < R) {
+            const int k = threadIdx.x;
+            const int e = __ldg(idx + tok * R + k);
+            const int sl = __ldg(slot_row + tok * R + k);
+            long long o = -1;
+            if ((unsigned)e < (unsigned)E && sl >= 0) {
+                const int p = e / Er;
+                const int c = __ldg(csend_off + (size_t)p * (N + 1) + s) +
+                              (sl - __ldg(send_off + (size_t)s * (N + 1) + p));
+                if (c >= 0 && c < cap) o = ((long long)p * cap + c) * H;
+            }
+            src[k] = o;
+            wk[k] = __ldg(w + tok * R + k);
+        }
+        __syncthreads();
+        for (int part = threadIdx.x; part < cpr; part += blockDim.x) {
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int k0 = 0; k0 < R; k0 += kReduceGroup) {
+                uint4 v[kReduceGroup];
+#pragma unroll
+                for (int u = 0; u < kReduceGroup; ++u) {
+                    const int k = k0 + u;
+                    if (k < R && src[k] >= 0)
+                        v[u] = __ldcs(reinterpret_cast<const uint4 *>(csend + src[k]) + part);
+                }
+#pragma unroll
+                for (int u = 0; u < kReduceGroup; ++u) {
+                    const int k = k0 + u;
+                    if (k < R && src[k] >= 0) fma8(acc, wk[k], v[u]);
+                }
+            }
+            uint4 o;
+            o.x = pack_bf16x2(acc[0], acc[1]);
+            o.y = pack_bf16x2(acc[2], acc[3]);
+            o.z = pack_bf16x2(acc[4], acc[5]);
+            o.w = pack_bf16x2(acc[6], acc[7]);
+            reinterpret_cast<uint4 *>(out + tok * H)[part] = o;
+        }
+        __syncthreads();
+    }
+}
+
+cudaError_t launch_combine_reduce(const moe_shape &sh, int cap, const uint16_t *csend,
+                                  const int32_t *idx, const float *w, const int32_t *slot_row,
+                                  const int32_t *send_off, const int32_t *csend_off,
+                                  uint16_t *out, cudaStream_t st) {
+    const long long ntok = (long long)sh.N * sh.T;
+    if (ntok == 0) return cudaSuccess;
+    const long long cap_blocks = (long long)sm_count() * (2048 / kReduceThreads);
+    const int grid = (int)(ntok < cap_blocks ? ntok : cap_blocks);
+    k_combine_reduce<<<grid, kReduceThreads, 0, st>>>(sh.N, sh.T, sh.E, sh.R, sh.H, cap, csend,
+                                                      idx, w, slot_row, send_off, csend_off, out);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ expert stand-in
+//
+// Not part of the timed path.  One warp per grouped row (grid-stride over
+// N*cap rows, rows past the received count skipped); y = bf16_rn((dq * scale)
+// * s_e) with fp32 multiplies.
+__device__ __forceinline__ float e4m3_to_float(uint8_t c) {
+    const __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)c, __NV_E4M3);
+    return __half2float(__half(h));
+}
+
+__global__ void __launch_bounds__(256)
+    k_expert_standin(int N, int E, int H, int cap, int mode, const uint8_t *__restrict__ grp_q,
+                     const float *__restrict__ grp_s, const int32_t *__restrict__ grp_off,
+                     uint16_t *__restrict__ y) {
+    const int lane = threadIdx.x & 31, Er = E / N, Sb = H >> 7;
+    const long long nrows = (long long)N * cap;
+    const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
+    for (long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+         row < nrows; row += nwarps) {
+        const int r = (int)(row / cap), g = (int)(row - (long long)r * cap);
+        const int32_t *go = grp_off + (size_t)r * (Er + 1);
+        if (g >= __ldg(go + Er)) continue;
+        const int e = r * Er + find_run(go, Er, g);
+        const float se = mode == 0 ? 1.0f : (e % 3 == 0 ? 0.5f : (e % 3 == 1 ? 1.0f : 2.0f));
+        const uint8_t *q = grp_q + row * H;
+        for (int c = lane; c < (H >> 4); c += 32) {
+            const uint4 qv = *reinterpret_cast<const uint4 *>(q + c * 16);
+            const float sc = __ldg(grp_s + row * Sb + (c >> 3));
+            const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+            uint32_t o[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const uint32_t word = qw[u >> 1] >> ((u & 1) * 16);
+                const float a = __fmul_rn(__fmul_rn(e4m3_to_float((uint8_t)(word & 0xff)), sc), se);
+                const float b =
+                    __fmul_rn(__fmul_rn(e4m3_to_float((uint8_t)((word >> 8) & 0xff)), sc), se);
+                o[u] = pack_bf16x2(a, b);
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(y + row * H + c * 16);
+            dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+            dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+    }
+}
+
+cudaError_t launch_expert_standin(const moe_shape &sh, int cap, int mode, const uint8_t *grp_q,
+                                  const float *grp_s, const int32_t *grp_off, uint16_t *y,
+                                  cudaStream_t st) {
+    const long long nrows = (long long)sh.N * cap;
+    if (nrows == 0) return cudaSuccess;
+    const long long need = (nrows + 7) / 8;
+    const long long cap_blocks = (long long)sm_count() * 8;
+    const int grid = (int)(need < cap_blocks ? need : cap_blocks);
+    k_expert_standin<<<grid, 256, 0, st>>>(sh.N, sh.E, sh.H, cap, mode, grp_q, grp_s, grp_off, y);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ e4m3 encoder
+//
+// The same conversion as the quantiser (pairs through
+// __nv_cvt_float2_to_fp8x2, saturating, round to nearest even).
+__global__ void k_e4m3_encode(const float *__restrict__ v, uint8_t *__restrict__ out,
+                              long long n) {
+    const long long npairs = (n + 1) / 2;
+    for (long long p = (long long)blockIdx.x * blockDim.x + threadIdx.x; p < npairs;
+         p += (long long)gridDim.x * blockDim.x) {
+        const long long i = 2 * p;
+        const float a = v[i];
+        const float b = i + 1 < n ? v[i + 1] : 0.0f;
+        const uint32_t c =
+            (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+        out[i] = (uint8_t)(c & 0xff);
+        if (i + 1 < n) out[i + 1] = (uint8_t)(c >> 8);
+    }
+}
+
+cudaError_t launch_e4m3_encode(const float *v, uint8_t *out, int64_t n, cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    const long long need = ((n + 1) / 2 + 255) / 256;
+    const long long cap_blocks = (long long)sm_count() * 8;
+    const int grid = (int)(need < cap_blocks ? need : cap_blocks);
+    k_e4m3_encode<<<grid, 256, 0, st>>>(v, out, n);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,48 @@
+// launch.h -- internal launchers behind the C ABI (arguments already
+// validated by api.cu; all pointers device memory, all calls asynchronous).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "moeroute.h"
+
+namespace moe {
+
+cudaError_t launch_route_count(const moe_shape &sh, const int32_t *idx, int32_t *cnt,
+                               int32_t *send_off, int32_t *eso, int32_t *slot_row,
+                               int32_t *status, cudaStream_t st);
+
+cudaError_t launch_exchange(const moe_shape &sh, int cap, const int32_t *cnt,
+                            const int32_t *send_off, int32_t *grp_off, int32_t *seg_off,
+                            int32_t *csend_off, int32_t *m_sizes, int32_t *status,
+                            cudaStream_t st);
+
+cudaError_t launch_quant_pack(const moe_shape &sh, const uint16_t *x, const int32_t *slot_row,
+                              uint8_t *send_q, float *send_s, int32_t *send_tok, cudaStream_t st);
+
+cudaError_t launch_dispatch_pull(const moe_shape &sh, int cap, const uint8_t *send_q,
+                                 const float *send_s, const int32_t *send_tok,
+                                 const int32_t *eso, const int32_t *seg_off, uint8_t *grp_q,
+                                 float *grp_s, int32_t *grp_src, int32_t *status, cudaStream_t st);
+
+cudaError_t launch_combine_pack(const moe_shape &sh, int cap, const uint16_t *y,
+                                const int32_t *eso, const int32_t *send_off,
+                                const int32_t *seg_off, const int32_t *csend_off, uint16_t *csend,
+                                int32_t *status, cudaStream_t st);
+
+cudaError_t launch_combine_reduce(const moe_shape &sh, int cap, const uint16_t *csend,
+                                  const int32_t *idx, const float *w, const int32_t *slot_row,
+                                  const int32_t *send_off, const int32_t *csend_off,
+                                  uint16_t *out, cudaStream_t st);
+
+cudaError_t launch_expert_standin(const moe_shape &sh, int cap, int mode, const uint8_t *grp_q,
+                                  const float *grp_s, const int32_t *grp_off, uint16_t *y,
+                                  cudaStream_t st);
+
+cudaError_t launch_e4m3_encode(const float *v, uint8_t *out, int64_t n, cudaStream_t st);
+
+// SM count of the current device (cached per device).
+int sm_count();
+
+}  // namespace moe

@@ -1,0 +1,168 @@
+// route.cu -- per-expert counting, exclusive scans and the routing-info
+// exchange ("Enabling trillion-parameter models on AWS EFA", sections "Send
+// and receive buffers" and "Dispatch and combine").
+//
+// k_route_count: one 1024-thread block per rank, as the page describes
+//   (counts accumulated with shared-memory atomics inside a single block,
+//   then a cumulative sum).  The stable slot of every (t, k) is found chunk
+//   by chunk: __match_any_sync gives each lane its rank among equal experts
+//   in its warp, a per-(expert, warp) table scanned across warps gives the
+//   rank among earlier warps of the chunk, and a running count per expert
+//   carries the earlier chunks.  The result equals "expert offset + number of
+//   earlier assignments with the same expert", independent of atomic order.
+//
+// k_exchange: one block per receiver; a block scan over the Er*N counts in
+//   (local expert, sender) order gives seg_off / grp_off / m_sizes, and a
+//   second scan over senders gives csend_off.
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+
+constexpr int kRouteThreads = 1024;
+
+__global__ void __launch_bounds__(kRouteThreads, 1)
+    k_route_count(int N, int T, int E, int R, const int32_t *__restrict__ idx,
+                  int32_t *__restrict__ cnt_out, int32_t *__restrict__ send_off,
+                  int32_t *__restrict__ eso_out, int32_t *__restrict__ slot_row,
+                  int32_t *__restrict__ status) {
+    extern __shared__ int smem[];
+    int *cnt = smem;           // [E] counts
+    int *base = cnt + E;       // [E] exclusive scan of counts
+    int *run = base + E;       // [E] assignments seen in earlier chunks
+    int *ctot = run + E;       // [E] assignments in the current chunk
+    unsigned short *tab = reinterpret_cast<unsigned short *>(ctot + E);  // [E][32]
+    __shared__ int wsum[32];
+    __shared__ int total;
+
+    const int s = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nw = blockDim.x >> 5;
+    const int TR = T * R, Er = E / N;
+    const int32_t *id = idx + (size_t)s * TR;
+
+    for (int e = tid; e < E; e += blockDim.x) {
+        cnt[e] = 0;
+        run[e] = 0;
+    }
+    for (int i = tid; i < E * 32; i += blockDim.x) tab[i] = 0;
+    __syncthreads();
+
+    // 1. counts with shared-memory atomics
+    int bad = 0;
+    for (int i = tid; i < TR; i += blockDim.x) {
+        int e = __ldg(id + i);
+        if ((unsigned)e < (unsigned)E)
+            atomicAdd(&cnt[e], 1);
+        else
+            bad = 1;
+    }
+    if (__syncthreads_or(bad) && tid == 0) flag(status, MOE_ST_BAD_EXPERT);
+
+    // 2. exclusive scan over experts (E <= blockDim.x: one expert per thread)
+    int v = tid < E ? cnt[tid] : 0;
+    int incl = block_inclusive_scan(v, wsum, &total);
+    if (tid < E) {
+        base[tid] = incl - v;
+        cnt_out[(size_t)s * E + tid] = v;
+        eso_out[(size_t)s * (E + 1) + tid] = incl - v;
+    }
+    if (tid == 0) eso_out[(size_t)s * (E + 1) + E] = total;
+    __syncthreads();
+    for (int p = tid; p <= N; p += blockDim.x)
+        send_off[(size_t)s * (N + 1) + p] = p < N ? base[p * Er] : total;
+
+    // 3. stable slots, one chunk of blockDim.x assignments at a time
+    const unsigned lt = (1u << lane) - 1u;
+    for (int c0 = 0; c0 < TR; c0 += blockDim.x) {
+        const int i = c0 + tid;
+        const int e = i < TR ? __ldg(id + i) : -1;
+        const bool good = (unsigned)e < (unsigned)E;
+        const unsigned peers = __match_any_sync(kFull, good ? e : -1);
+        const int rank = __popc(peers & lt);
+        if (good && rank == 0) tab[e * 32 + warp] = (unsigned short)__popc(peers);
+        __syncthreads();
+        for (int x = warp; x < E; x += nw) {
+            int c = lane < nw ? tab[x * 32 + lane] : 0;
+            int ci = warp_inclusive_scan(c);
+            if (lane < nw) tab[x * 32 + lane] = (unsigned short)(ci - c);
+            if (lane == 31) ctot[x] = ci;
+        }
+        __syncthreads();
+        if (i < TR) slot_row[(size_t)s * TR + i] = good ? base[e] + run[e] + tab[e * 32 + warp] + rank : -1;
+        __syncthreads();
+        for (int x = warp; x < E; x += nw) {
+            if (lane < nw) tab[x * 32 + lane] = 0;
+            if (lane == 0) run[x] += ctot[x];
+        }
+        __syncthreads();
+    }
+}
+
+__global__ void __launch_bounds__(1024)
+    k_exchange(int N, int E, int cap, const int32_t *__restrict__ cnt,
+               const int32_t *__restrict__ send_off, int32_t *__restrict__ grp_off,
+               int32_t *__restrict__ seg_off, int32_t *__restrict__ csend_off,
+               int32_t *__restrict__ m_sizes, int32_t *__restrict__ status) {
+    __shared__ int wsum[32];
+    __shared__ int total;
+    __shared__ int excl[MOE_MAX_EXPERTS + 1];
+    const int r = blockIdx.x, tid = threadIdx.x, Er = E / N, F = Er * N;
+
+    // runs in (local expert j, sender s) order: f = j*N + s
+    const int j = tid / N, s = tid - (tid / N) * N;
+    const int v = tid < F ? __ldg(cnt + (size_t)s * E + r * Er + j) : 0;
+    const int incl = block_inclusive_scan(v, wsum, &total);
+    if (tid < F) {
+        excl[tid] = incl - v;
+        seg_off[(size_t)r * F + tid] = incl - v;  // [r][j][s]
+    }
+    const int recv = total;
+    if (tid == 0) excl[F] = recv;
+    __syncthreads();
+    if (tid <= Er) grp_off[(size_t)r * (Er + 1) + tid] = excl[tid * N];
+    if (tid < Er) m_sizes[(size_t)r * Er + tid] = excl[(tid + 1) * N] - excl[tid * N];
+    if (tid == 0 && recv > cap) flag(status, MOE_ST_CAPACITY);
+
+    // rows going back to each sender s, in sender order
+    const int w = tid < N ? __ldg(send_off + (size_t)tid * (N + 1) + r + 1) -
+                                __ldg(send_off + (size_t)tid * (N + 1) + r)
+                          : 0;
+    const int wi = block_inclusive_scan(w, wsum, &total);
+    if (tid < N) csend_off[(size_t)r * (N + 1) + tid] = wi - w;
+    if (tid == 0) csend_off[(size_t)r * (N + 1) + N] = total;
+}
+
+static size_t route_smem(int E) { return (size_t)E * 4 * sizeof(int) + (size_t)E * 32 * 2; }
+
+cudaError_t launch_route_count(const moe_shape &sh, const int32_t *idx, int32_t *cnt,
+                               int32_t *send_off, int32_t *eso, int32_t *slot_row,
+                               int32_t *status, cudaStream_t st) {
+    cudaError_t err = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
+    if (err != cudaSuccess) return err;
+    const size_t smem = route_smem(sh.E);
+    static int attr_dev = -1;
+    int dev = 0;
+    err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev != attr_dev) {
+        // room for the largest E once per device
+        err = cudaFuncSetAttribute(k_route_count, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)route_smem(MOE_MAX_EXPERTS));
+        if (err != cudaSuccess) return err;
+        attr_dev = dev;
+    }
+    k_route_count<<<sh.N, kRouteThreads, smem, st>>>(sh.N, sh.T, sh.E, sh.R, idx, cnt, send_off,
+                                                     eso, slot_row, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_exchange(const moe_shape &sh, int cap, const int32_t *cnt,
+                            const int32_t *send_off, int32_t *grp_off, int32_t *seg_off,
+                            int32_t *csend_off, int32_t *m_sizes, int32_t *status,
+                            cudaStream_t st) {
+    k_exchange<<<sh.N, 1024, 0, st>>>(sh.N, sh.E, cap, cnt, send_off, grp_off, seg_off, csend_off,
+                                      m_sizes, status);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

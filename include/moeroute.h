@@ -1,0 +1,231 @@
+/*
+ * moeroute.h -- C ABI of libmoeroute: MoE expert-parallel dispatch and
+ * combine for one GB300 (sm_103a), with the N expert-parallel ranks held as N
+ * slices of the one GPU's memory.
+ *
+ * The operations follow "Enabling trillion-parameter models on AWS EFA"
+ * (Perplexity blog):
+ *   - Introduction: dispatch splits each rank's tokens and sends each to the
+ *     ranks that host its experts; combine brings the expert outputs back and
+ *     takes each token's weighted average.
+ *   - "EFA-based MoE all-to-all": both are split into a send half and a
+ *     receive half so other work can run in between.
+ *   - "Send and receive buffers": per-expert token counts are exchanged first
+ *     so that every sender can lay out its writes contiguously per peer and
+ *     every receiver knows where each sender's tokens land; a rank receives
+ *     at most N*T*max(R, E/N) tokens.
+ *   - "Dispatch and combine": counting with shared-memory atomics in one
+ *     block, a cumulative sum to offsets, packing into contiguous per-peer
+ *     send buffers, receive-side offsets once all routing info is in, the
+ *     shuffle into the grouped-GEMM input, and a combine that packs outputs
+ *     per peer and accumulates the weighted average on the receiving side.
+ *   - "Evaluation: dispatch/combine latency": block-scaled fp8 dispatch and
+ *     bf16 combine.
+ *
+ * Notation: N ranks, T tokens per rank, E experts, R experts per token
+ * (top-k), H hidden size.  Er = E/N experts per rank; expert e lives on rank
+ * e / Er.  Sb = H/128 scale blocks per row.  cap = grouped rows per rank.
+ *
+ * Layout: every per-rank array is a slab [N][...] in one allocation; rank
+ * r's slice starts at r * (slice size).  All arrays are row-major and dense.
+ *   topk_idx        int32 [N][T][R]     expert ids chosen by the router
+ *   topk_w          float [N][T][R]     their combine weights
+ *   x               bf16  [N][T][H]     token activations (raw bf16 bits)
+ *   expert_count    int32 [N][E]        tokens rank s sends to expert e
+ *   send_off        int32 [N][N+1]      exclusive scan over peers
+ *   expert_send_off int32 [N][E+1]      exclusive scan over experts
+ *   slot_row        int32 [N][T][R]     send-buffer row of each assignment
+ *                                       (-1: expert id outside [0, E))
+ *   send_q          u8    [N][T*R][H]   fp8 e4m3 payload, per-peer contiguous
+ *   send_s          float [N][T*R][Sb]  per-block scales of each send row
+ *   send_tok        int32 [N][T*R]      source token of each send row
+ *   grp_off         int32 [N][Er+1]     first grouped row of each local
+ *                                       expert; grp_off[r][Er] = rows received
+ *   seg_off         int32 [N][Er][N]    grouped row where sender s's run of
+ *                                       local expert j starts
+ *   csend_off       int32 [N][N+1]      row in the combine send buffer where
+ *                                       the rows going back to s start
+ *   m_sizes         int32 [N][Er]       rows per local expert (GEMM sizes)
+ *   grp_q           u8    [N][cap][H]   grouped fp8 payload (GEMM input)
+ *   grp_s           float [N][cap][Sb]  grouped scales
+ *   grp_src         int32 [N][cap][2]   (source rank, source token) per row
+ *   y               bf16  [N][cap][H]   expert outputs, grouped layout
+ *   csend           bf16  [N][cap][H]   combine send buffer, per-destination
+ *                                       contiguous
+ *   out             bf16  [N][T][H]     combined output
+ *
+ * Ownership: every pointer is device memory owned by the caller (sized with
+ * moe_sizes_query).  The library allocates nothing and keeps no state
+ * between calls.  `stream` is a cudaStream_t (NULL = legacy default stream).
+ *
+ * Execution: calls only enqueue work on `stream` and never wait for the
+ * device, so a sequence of calls can be captured in a CUDA graph.  Order on
+ * the stream replaces the pages' receive-side waits and barriers.
+ *
+ * Errors: argument checks run on the host before anything is enqueued and
+ * return MOE_EINVAL; a failed launch returns MOE_ECUDA.  Faults found on the
+ * device are OR-ed into the int32 at `status` (device memory), which
+ * moe_route_count clears first; read it after the stream has finished.  No
+ * kernel traps, asserts or waits without a bound.
+ */
+#ifndef MOEROUTE_H
+#define MOEROUTE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_OK 0
+#define MOE_EINVAL (-1)     /* bad shape, null or misaligned pointer */
+#define MOE_ENOTSUP (-2)    /* shape outside the supported limits below */
+#define MOE_ECUDA (-3)      /* a CUDA call or launch failed */
+
+#define MOE_ST_BAD_EXPERT 1 /* an expert id was outside [0, E): assignment skipped */
+#define MOE_ST_CAPACITY 2   /* a rank received more than cap rows: extra rows dropped */
+#define MOE_ST_TIMEOUT 4    /* a bounded wait inside a kernel gave up */
+
+/* Supported limits (MOE_ENOTSUP beyond them): 1 <= N <= E <= 1024, E % N == 0,
+ * 1 <= R <= min(E, 32), 0 <= T, T*R < 2^31, 128 <= H <= 65536 with
+ * H % 128 == 0, N*cap < 2^31. */
+#define MOE_MAX_EXPERTS 1024
+#define MOE_MAX_TOPK 32
+
+typedef struct {
+    int N;   /* ranks */
+    int T;   /* tokens per rank */
+    int E;   /* experts */
+    int R;   /* experts per token */
+    int H;   /* hidden size, multiple of 128 */
+    int cap; /* grouped rows per rank; 0 selects N*T*min(R, E/N), which holds
+                every routing whose R experts per token are distinct */
+} moe_shape;
+
+/* Byte sizes of every buffer for a shape (whole slab, all N ranks). */
+typedef struct {
+    int64_t cap;            /* effective grouped rows per rank */
+    int64_t send_rows;      /* T*R rows per rank */
+    int64_t bytes_x;        /* also bytes_out */
+    int64_t bytes_topk_idx; /* also topk_w, slot_row */
+    int64_t bytes_expert_count;
+    int64_t bytes_send_off; /* also csend_off */
+    int64_t bytes_expert_send_off;
+    int64_t bytes_grp_off;
+    int64_t bytes_seg_off;
+    int64_t bytes_m_sizes;
+    int64_t bytes_send_q;
+    int64_t bytes_send_s;
+    int64_t bytes_send_tok;
+    int64_t bytes_grp_q;
+    int64_t bytes_grp_s;
+    int64_t bytes_grp_src;
+    int64_t bytes_y;        /* also bytes_csend */
+} moe_sizes;
+
+/* Fill *out for *shape.  Host only.  MOE_EINVAL / MOE_ENOTSUP on a bad shape. */
+int moe_sizes_query(const moe_shape *shape, moe_sizes *out);
+
+/* Dispatch send, step 1 ("Dispatch and combine": per-expert counts with
+ * shared-memory atomics in one block per rank, then a cumulative sum).
+ * Clears *status.  One thread block per rank s:
+ *   expert_count[s][e]   = #{(t,k): topk_idx[s][t][k] == e}
+ *   expert_send_off[s][] = exclusive scan of expert_count[s][] (E+1 entries)
+ *   send_off[s][p]       = expert_send_off[s][p*Er]  (N+1 entries)
+ *   slot_row[s][t][k]    = expert_send_off[s][e] + number of earlier (t',k')
+ *                          of rank s, in flattened order t'*R+k', with the
+ *                          same expert; -1 (and MOE_ST_BAD_EXPERT) when the id
+ *                          is outside [0, E). */
+int moe_route_count(const moe_shape *shape, const int32_t *topk_idx, int32_t *expert_count,
+                    int32_t *send_off, int32_t *expert_send_off, int32_t *slot_row,
+                    int32_t *status, void *stream);
+
+/* Routing-information exchange and receive-side offsets ("Send and receive
+ * buffers"; "Dispatch and combine": once a rank has everyone's routing info
+ * it computes the offsets for dispatch and combine).  For receiver r and its
+ * local expert j (e = r*Er + j), with the runs ordered by j then sender s:
+ *   seg_off[r][j][s] = sum of expert_count[s'][e'] over all runs before (j, s)
+ *   grp_off[r][j]    = seg_off[r][j][0];  grp_off[r][Er] = rows r receives
+ *   m_sizes[r][j]    = sum_s expert_count[s][e]
+ *   csend_off[r][s]  = sum_{s' < s} (send_off[s'][r+1] - send_off[s'][r])
+ * Sets MOE_ST_CAPACITY when some rank receives more than cap rows. */
+int moe_exchange(const moe_shape *shape, const int32_t *expert_count, const int32_t *send_off,
+                 int32_t *grp_off, int32_t *seg_off, int32_t *csend_off, int32_t *m_sizes,
+                 int32_t *status, void *stream);
+
+/* Dispatch send, step 2: block-scaled fp8 quantisation fused with the pack
+ * ("Dispatch and combine"; "Evaluation": block-scaled fp8 dispatch).  Per
+ * token and 128-element block: amax = max|x|, scale = amax/448 (fp32
+ * division), q = e4m3 round-to-nearest-even with saturation of x/scale (fp32
+ * division); amax == 0 gives scale 0 and zero bytes.  The token's payload,
+ * scales and id go to send rows slot_row[s][t][k] for every k with a valid
+ * slot.  Rows of send_q no assignment maps to are left untouched. */
+int moe_dispatch_send(const moe_shape *shape, const uint16_t *x_bf16, const int32_t *slot_row,
+                      uint8_t *send_q, float *send_s, int32_t *send_tok, int32_t *status,
+                      void *stream);
+
+/* Dispatch receive: shuffle into the expert-grouped layout handed to the
+ * grouped GEMM ("Dispatch and combine": tokens are shuffled from the receive
+ * buffer into the grouped-GEMM input).  For every receiver r, local expert j
+ * and sender s, the run of expert_count[s][e] rows that s packed for e
+ * (from send row expert_send_off[s][e]) is copied to grouped rows from
+ * seg_off[r][j][s], with its scales; grp_src gets (s, source token).  The
+ * exchange is a device-side pull from the sender's slice.  Rows at or beyond
+ * cap are dropped (MOE_ST_CAPACITY was set by moe_exchange).  Rows >= the
+ * received count are left untouched. */
+int moe_dispatch_recv(const moe_shape *shape, const uint8_t *send_q, const float *send_s,
+                      const int32_t *send_tok, const int32_t *expert_count,
+                      const int32_t *expert_send_off, const int32_t *seg_off, uint8_t *grp_q,
+                      float *grp_s, int32_t *grp_src, int32_t *status, void *stream);
+
+/* Combine send: expert rank r copies each run of outputs (grouped rows from
+ * seg_off[r][j][s]) into its combine send buffer at
+ *   csend_off[r][s] + (expert_send_off[s][e] - send_off[s][r])
+ * so the rows going back to s are contiguous and in s's own send order ("one
+ * write per peer").  A row whose grouped position was dropped is sent as
+ * zeros; a row at or beyond cap in csend is dropped. */
+int moe_combine_send(const moe_shape *shape, const uint16_t *y_bf16, const int32_t *expert_count,
+                     const int32_t *expert_send_off, const int32_t *send_off,
+                     const int32_t *seg_off, const int32_t *csend_off, uint16_t *csend,
+                     int32_t *status, void *stream);
+
+/* Combine receive: weighted average accumulated on the receiving side
+ * ("Dispatch and combine"; the evaluation notes this receive-side-only
+ * accumulation).  For token t of rank s:
+ *   acc = 0; for k = 0..R-1: acc = fmaf(topk_w[s][t][k], row_k, acc)
+ *   out[s][t] = bf16 round-to-nearest-even(acc)
+ * row_k is read from rank p = e/Er's combine send buffer at
+ *   csend_off[p][s] + (slot_row[s][t][k] - send_off[s][p]).
+ * Skipped (invalid id) and dropped (>= cap) assignments contribute nothing. */
+int moe_combine_recv(const moe_shape *shape, const uint16_t *csend, const int32_t *topk_idx,
+                     const float *topk_w, const int32_t *slot_row, const int32_t *send_off,
+                     const int32_t *csend_off, uint16_t *out_bf16, int32_t *status,
+                     void *stream);
+
+/* Stand-in for the grouped GEMM between dispatch and combine (the pages'
+ * expert computation is out of scope here):
+ *   y = bf16_rn((e4m3_decode(q) * scale) * s_e),  fp32 multiplies,
+ * s_e = 1 for mode 0 (identity) and 2^((e mod 3) - 1) for mode 1 (a fixed
+ * per-expert scale).  Writes the received rows of every rank; other rows of
+ * y are left untouched. */
+int moe_expert_standin(const moe_shape *shape, int mode, const uint8_t *grp_q,
+                       const float *grp_s, const int32_t *grp_off, uint16_t *y_bf16,
+                       void *stream);
+
+/* The fp32 -> e4m3 conversion the quantiser applies (round to nearest even,
+ * saturate to +-448), element-wise over n values; exposed so the encoder can
+ * be compared with other implementations. */
+int moe_e4m3_encode(const float *v, uint8_t *out, int64_t n, void *stream);
+
+/* Static description of an error code or status bit set. */
+const char *moe_strerror(int code);
+
+/* Library version, (major << 16) | minor. */
+int moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOEROUTE_H */

@@ -1,0 +1,83 @@
+"""Host-side logic of bench.py without a GPU: the reference arm (the CPU
+oracle) prints a well-formed line, the byte model matches the documented
+formulas, and the max-over-ranks reduction works across two gloo ranks."""
+from __future__ import annotations
+
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from combine_expert_count_gb300 import workloads as W  # noqa: E402
+
+
+def test_algorithmic_bytes_match_formulas():
+    w = W.CONFIGS["dsv3_decode"]
+    b = bench.algorithmic_bytes(w, w.A)
+    assert round(b["dispatch"] / 1e6, 1) == 392.8
+    assert round(b["combine"] / 1e6, 1) == 734.1
+    per = b["per_kernel"]
+    assert per["combine_send"] == 4 * w.A * w.H
+    assert per["dispatch_send"] > 2 * w.N * w.T * w.H
+
+
+def test_reference_arm_prints_one_json_line():
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0")
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--config", "tiny", "--steps", "2", "--warmup", "1", "--ref-tokens", "4"],
+                         capture_output=True, text=True, env=env, timeout=300, check=True).stdout
+    lines = [ln for ln in out.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
+    assert d["higher_is_better"] is False and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_reference_arm_other_ranks_do_nothing():
+    env = dict(os.environ, WORLD_SIZE="2", RANK="1")
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--config", "tiny", "--steps", "1", "--warmup", "1"],
+                         capture_output=True, text=True, env=env, timeout=120, check=True).stdout
+    assert out.strip() == ""
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    import torch.distributed as dist
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
+                            world_size=world)
+    try:
+        bench.barrier(world)
+        v = bench.max_over_ranks(10.0 + rank, world)
+        q.put((rank, v))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_two_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    assert got == [(0, 11.0), (1, 11.0)]
