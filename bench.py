@@ -1,9 +1,13 @@
 #!/usr/bin/env python3
 """Dispatch + combine benchmark on one GB300.
 
-One step = one MoE layer's hot path over one batch: route_count, exchange,
-dispatch_send, dispatch_recv (dispatch) and combine_send, combine_recv
-(combine), each a launch of libmoeroute through its C ABI.  The grouped-GEMM
+One step = one MoE layer's hot path over one batch: route (route_count and
+exchange in one launch), dispatch_send, dispatch_recv (dispatch) and
+combine_send, combine_recv (combine), run through libmoeroute's C ABI as the
+two pipelined calls moe_dispatch and moe_combine (the same kernels, ordered
+by chunks of sender ranks so each consumer reads its producer's rows from
+L2); a second pass times the separate calls one by one for the per-kernel
+breakdown.  The grouped-GEMM
 stand-in runs once before timing (its output is the same every step) and is
 not timed.  Inputs are resident in HBM when timing starts; L2 is flushed
 (512 MiB write) before every step, outside the timed window.
@@ -38,9 +42,8 @@ UNIT = "us/layer"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 512 << 20
-KERNELS = ("route_count", "exchange", "dispatch_send", "dispatch_recv", "combine_send",
-           "combine_recv")
-KERNEL_SYMBOL = {"route_count": "k_route_count", "exchange": "k_exchange",
+KERNELS = ("route", "dispatch_send", "dispatch_recv", "combine_send", "combine_recv")
+KERNEL_SYMBOL = {"route": "k_route (route_count + exchange)",
                  "dispatch_send": "k_quant_pack", "dispatch_recv": "k_row_shuffle<DispatchMap>",
                  "combine_send": "k_row_shuffle<CombineMap>", "combine_recv": "k_combine_reduce"}
 
@@ -303,11 +306,15 @@ def run_ours(args) -> None:
 
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
+    tens = buf.tensors(x=x, topk_idx=idx, topk_w=wt)
+    pipelined = (
+        lambda: m.moe_dispatch(sh, tens, args.chunks),
+        lambda: m.moe_combine(sh, tens, args.chunks),
+    )
     calls = (
-        lambda: m.moe_route_count(sh, idx, buf.expert_count, buf.send_off, buf.expert_send_off,
-                                  buf.slot_row, buf.status),
-        lambda: m.moe_exchange(sh, buf.expert_count, buf.send_off, buf.grp_off, buf.seg_off,
-                               buf.csend_off, buf.m_sizes, buf.status),
+        lambda: m.moe_route(sh, idx, buf.expert_count, buf.send_off, buf.expert_send_off,
+                            buf.slot_row, buf.grp_off, buf.seg_off, buf.csend_off, buf.m_sizes,
+                            buf.status),
         lambda: m.moe_dispatch_send(sh, x, buf.slot_row, buf.send_q, buf.send_s, buf.send_tok,
                                     buf.status),
         lambda: m.moe_dispatch_recv(sh, buf.send_q, buf.send_s, buf.send_tok, buf.expert_count,
@@ -321,30 +328,37 @@ def run_ours(args) -> None:
     )
 
     def step(ev=None):
+        """The five calls one by one (an event after each when timing them)."""
         for i, c in enumerate(calls):
             c()
             if ev is not None:
                 ev[i + 1].record(stream)
 
+    def step_pipelined():
+        """The same work as step(): moe_dispatch then moe_combine."""
+        for c in pipelined:
+            c()
+
     K = args.steps
     W_ = max(args.warmup, 3)
 
-    # The six calls captured once as a CUDA graph (the library never waits on
-    # the host, so the sequence captures); replays run exactly these kernels.
+    # The headline step is the pipelined form (moe_dispatch, moe_combine),
+    # captured once as a CUDA graph (the library never waits on the host, so
+    # the sequence captures); replays run exactly those kernels.
     graph = None
     if not args.eager:
         cap_stream = torch.cuda.Stream(device=dev)
         cap_stream.wait_stream(stream)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=cap_stream):
-            step()
+            step_pipelined()
         torch.cuda.synchronize()
 
     def run_once():
         if graph is not None:
             graph.replay()
         else:
-            step()
+            step_pipelined()
 
     for _ in range(W_):
         flush.zero_()
@@ -429,8 +443,8 @@ def run_ours(args) -> None:
     # dominant kernel: the largest share of the step
     dom = max(("dispatch_send", "dispatch_recv", "combine_send", "combine_recv"), key=avg.get)
     dom_gbs = nbytes["per_kernel"][dom] / (avg[dom] * 1e-3) / 1e9
-    disp_us = sum(avg[n] for n in KERNELS[:4]) * 1000
-    comb_us = sum(avg[n] for n in KERNELS[4:]) * 1000
+    disp_us = sum(avg[n] for n in KERNELS[:3]) * 1000
+    comb_us = sum(avg[n] for n in KERNELS[3:]) * 1000
     line = {
         "metric": METRIC, "value": round(us, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": W_, "ms_per_step": round(mean_step_ms, 5),
@@ -443,8 +457,10 @@ def run_ours(args) -> None:
                    "N": w.N, "T": w.T, "H": w.H, "E": w.E, "R": w.R, "cap": buf.cap,
                    "l2": "flushed before every step (512 MiB write, outside the timed window)",
                    "parallelism": "ranks simulated as slices of one GPU; replicas across GPUs"},
-        "timing": "CUDA-graph replay of the six calls" if graph is not None else "eager launches",
-        "eager_us_with_kernel_events": round(eager_ms * 1000, 2),
+        "timing": ("CUDA-graph replay of moe_dispatch + moe_combine" if graph is not None
+                   else "eager moe_dispatch + moe_combine"),
+        "chunks": args.chunks,
+        "separate_calls_us_with_kernel_events": round(eager_ms * 1000, 2),
         "dispatch_us": round(disp_us, 2), "combine_us": round(comb_us, 2),
         "achieved_gbs": round(achieved, 1),
         "frac_of_peak": round(achieved / peak, 4), "peak_gbs": peak, "peak_kind": peak_kind,
@@ -479,6 +495,8 @@ def main() -> None:
     ap.add_argument("--config", default="dsv3_decode")
     ap.add_argument("--cap", type=int, default=0,
                     help="grouped rows per rank (0: N*T*min(R,E/N), the library default)")
+    ap.add_argument("--chunks", type=int, default=0,
+                    help="sender chunks of the pipelined calls (0: sized to L2, 1: none)")
     ap.add_argument("--eager", action="store_true",
                     help="time eager launches instead of CUDA-graph replays")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")

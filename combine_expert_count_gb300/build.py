@@ -48,8 +48,8 @@ def _fingerprint() -> str:
     return h.hexdigest()
 
 
-def _compile(src: str, extra: list[str]) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+def _compile(src: str, extra: list[str], bdir: str) -> str:
+    obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
     cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
@@ -57,31 +57,38 @@ def _compile(src: str, extra: list[str]) -> str:
     return obj
 
 
-def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:
-    """Compile and link; skipped when sources and flags are unchanged."""
+def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None,
+          out: str | None = None) -> str:
+    """Compile and link; skipped when sources and flags are unchanged.
+
+    ``extra`` adds nvcc flags (e.g. -D tuning macros); ``out`` writes the
+    library elsewhere (objects go to a build folder of their own)."""
     extra = list(extra or [])
-    os.makedirs(BUILD, exist_ok=True)
-    stamp = os.path.join(BUILD, "libmoeroute.stamp")
+    lib = out or LIB
+    bdir = BUILD if out is None else os.path.join(BUILD, "v_" + hashlib.sha256(
+        lib.encode()).hexdigest()[:12])
+    os.makedirs(bdir, exist_ok=True)
+    stamp = os.path.join(bdir, "libmoeroute.stamp")
     fp = _fingerprint() + "|" + " ".join(extra)
-    if not force and os.path.exists(LIB) and os.path.exists(stamp):
+    if not force and os.path.exists(lib) and os.path.exists(stamp):
         with open(stamp) as f:
             if f.read() == fp:
-                return LIB
+                return lib
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
+        objs = list(ex.map(lambda s: _compile(s, extra, bdir), srcs))
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
            "-Xlinker", "-rpath,/usr/local/cuda/lib64"]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     with open(stamp, "w") as f:
         f.write(fp)
     if verbose:
-        print(f"built {LIB}", file=sys.stderr)
-    return LIB
+        print(f"built {lib}", file=sys.stderr)
+    return lib
 
 
 if __name__ == "__main__":

@@ -138,6 +138,24 @@ int moe_exchange(const moe_shape *sh, const int32_t *expert_count, const int32_t
                                         csend_off, m_sizes, status, as_stream(stream)));
 }
 
+int moe_route(const moe_shape *sh, const int32_t *topk_idx, int32_t *expert_count,
+              int32_t *send_off, int32_t *expert_send_off, int32_t *slot_row, int32_t *grp_off,
+              int32_t *seg_off, int32_t *csend_off, int32_t *m_sizes, int32_t *status,
+              void *stream) {
+    moe_sizes z;
+    int rc = moe_sizes_query(sh, &z);
+    if (rc != MOE_OK) return rc;
+    if (!ok_ptr(topk_idx, z.bytes_topk_idx) || !ok_ptr(slot_row, z.bytes_topk_idx) ||
+        !ok_ptr(expert_count, z.bytes_expert_count) || !ok_ptr(send_off, z.bytes_send_off) ||
+        !ok_ptr(expert_send_off, z.bytes_expert_send_off) || !ok_ptr(grp_off, z.bytes_grp_off) ||
+        !ok_ptr(seg_off, z.bytes_seg_off) || !ok_ptr(csend_off, z.bytes_send_off) ||
+        !ok_ptr(m_sizes, z.bytes_m_sizes) || !ok_ptr(status, 4))
+        return MOE_EINVAL;
+    return cuda_rc(moe::launch_route(*sh, (int)z.cap, topk_idx, expert_count, send_off,
+                                     expert_send_off, slot_row, grp_off, seg_off, csend_off,
+                                     m_sizes, status, as_stream(stream)));
+}
+
 int moe_dispatch_send(const moe_shape *sh, const uint16_t *x_bf16, const int32_t *slot_row,
                       uint8_t *send_q, float *send_s, int32_t *send_tok, int32_t *status,
                       void *stream) {
@@ -148,7 +166,7 @@ int moe_dispatch_send(const moe_shape *sh, const uint16_t *x_bf16, const int32_t
         !ok_ptr(send_q, z.bytes_send_q) || !ok_ptr(send_s, z.bytes_send_s) ||
         !ok_ptr(send_tok, z.bytes_send_tok) || !ok_ptr(status, 4))
         return MOE_EINVAL;
-    return cuda_rc(moe::launch_quant_pack(*sh, x_bf16, slot_row, send_q, send_s, send_tok,
+    return cuda_rc(moe::launch_quant_pack(*sh, x_bf16, slot_row, send_q, send_s, send_tok, status,
                                           as_stream(stream)));
 }
 

@@ -13,13 +13,18 @@ namespace moe {
 
 // ------------------------------------------------------------ combine reduce
 //
-// One 128-thread block per token (grid-stride over tokens).  Threads 0..R-1
+// One small block per token (grid-stride over tokens).  Threads 0..R-1
 // resolve where each of the token's R rows sits (rank p = e/Er, row
 // csend_off[p][s] + slot - send_off[s][p]) into shared memory; then every
 // thread takes 16-byte chunks of the row, issues the R loads, and folds them
 // into fp32 accumulators with one fused multiply-add per slot in slot order
 // k = 0..R-1, rounding once to bf16 at the end.
-constexpr int kReduceThreads = 128;
+#ifndef MOE_REDUCE_THREADS
+#define MOE_REDUCE_THREADS 64
+#endif
+// 64 threads per token keeps a DeepSeek-V3-sized batch (2048 tokens) within
+// one wave of resident blocks.
+constexpr int kReduceThreads = MOE_REDUCE_THREADS;
 constexpr int kReduceGroup = 8;  // row loads kept in flight per chunk
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -40,7 +45,7 @@ __device__ __forceinline__ void fma8(float (&acc)[8], float w, const uint4 &v) {
 }
 
 __global__ void __launch_bounds__(kReduceThreads)
-    k_combine_reduce(int N, int T, int E, int R, int H, int cap,
+    k_combine_reduce(int N, int T, int E, int R, int H, int cap, long long tok0, long long tok1,
                      const uint16_t *__restrict__ csend, const int32_t *__restrict__ idx,
                      const float *__restrict__ w, const int32_t *__restrict__ slot_row,
                      const int32_t *__restrict__ send_off, const int32_t *__restrict__ csend_off,
@@ -48,9 +53,8 @@ __global__ void __launch_bounds__(kReduceThreads)
     __shared__ long long src[MOE_MAX_TOPK];  // element offset of row k in csend, -1: skip
     __shared__ float wk[MOE_MAX_TOPK];
     const int Er = E / N, cpr = H >> 3;
-    const long long ntok = (long long)N * T;
-    for (long long tok = blockIdx.x; tok < ntok; tok += gridDim.x) {
-        const int s = (int)(tok / T);
+    for (long long tok = tok0 + blockIdx.x; tok < tok1; tok += gridDim.x) {
+        const int s = (int)div_nonneg(tok, T);
         if (threadIdx.x < R) {
             const int k = threadIdx.x;
             const int e = __ldg(idx + tok * R + k);
@@ -96,14 +100,14 @@ __global__ void __launch_bounds__(kReduceThreads)
 cudaError_t launch_combine_reduce(const moe_shape &sh, int cap, const uint16_t *csend,
                                   const int32_t *idx, const float *w, const int32_t *slot_row,
                                   const int32_t *send_off, const int32_t *csend_off,
-                                  uint16_t *out, cudaStream_t st) {
-    const long long ntok = (long long)sh.N * sh.T;
-    if (ntok == 0) return cudaSuccess;
-    const long long cap_blocks = (long long)sm_count() * (2048 / kReduceThreads);
-    const int grid = (int)(ntok < cap_blocks ? ntok : cap_blocks);
-    k_combine_reduce<<<grid, kReduceThreads, 0, st>>>(sh.N, sh.T, sh.E, sh.R, sh.H, cap, csend,
-                                                      idx, w, slot_row, send_off, csend_off, out);
-    return cudaGetLastError();
+                                  uint16_t *out, cudaStream_t st, long long tok0, long long tok1) {
+    if (tok1 < 0) tok1 = (long long)sh.N * sh.T;
+    const long long ntok = tok1 - tok0;
+    if (ntok <= 0) return cudaSuccess;
+    const int grid = (int)(ntok < (1LL << 30) ? ntok : (1LL << 30));
+    return launch_kernel(k_combine_reduce, dim3((unsigned)grid), dim3(kReduceThreads), 0, st,
+                         sh.N, sh.T, sh.E, sh.R, sh.H, cap, tok0, tok1, csend, idx, w, slot_row,
+                         send_off, csend_off, out);
 }
 
 // ------------------------------------------------------------ expert stand-in

@@ -119,12 +119,33 @@ __device__ __forceinline__ void bulk_wait_read() {
     asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 
+// Order this thread's generic-proxy writes to shared memory before later
+// async-proxy (bulk copy) reads of it.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Wait until every committed bulk group has completed (writes performed).
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // ------------------------------------------------------------ misc
+
+// Round a shared-memory pointer up to a 128-byte boundary.
+template <class T>
+__device__ __forceinline__ T *align128(T *p) {
+    return reinterpret_cast<T *>((reinterpret_cast<uintptr_t>(p) + 127) &
+                                 ~static_cast<uintptr_t>(127));
+}
+
+// a / b for non-negative a, b > 0: a 32-bit division when both fit (a 64-bit
+// division costs dozens of instructions).
+__device__ __forceinline__ long long div_nonneg(long long a, long long b) {
+    if (a <= 0xffffffffLL && b <= 0xffffffffLL)
+        return (long long)((unsigned)a / (unsigned)b);
+    return a / b;
+}
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -141,6 +162,18 @@ __device__ __forceinline__ int find_run(const int32_t *__restrict__ off, int E, 
             hi = mid;
     }
     return lo;
+}
+
+// Launch `kern` on `st` with the given geometry.
+template <class... KArgs, class... Args>
+inline cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
 }  // namespace moe

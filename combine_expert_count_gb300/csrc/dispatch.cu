@@ -10,93 +10,203 @@
 
 namespace moe {
 
-// ------------------------------------------------------------ quant + pack
-//
-// One thread per 16 consecutive elements of a token row: two 16-byte loads
-// of x, 8 lanes per 128-element block (amax by xor-shuffles within the
-// group), scale = amax/448 and q = e4m3_satfinite_rn(x/scale) with IEEE fp32
-// divisions, then one 16-byte store into each of the token's R send rows.
-// A warp covers 512 contiguous bytes of a row, so every store is a full
-// coalesced line.
-constexpr int kQuantThreads = 256;
-
+// The conversion: two fp32 values to two e4m3 bytes (first value in the
+// low byte), round to nearest even, saturating to +-448.
 __device__ __forceinline__ uint32_t cvt_pair(float a, float b) {
     return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
 }
 
-__global__ void __launch_bounds__(kQuantThreads)
-    k_quant_pack(int T, int R, int H, long long nchunks, const uint16_t *__restrict__ x,
-                 const int32_t *__restrict__ slot_row, uint8_t *__restrict__ send_q,
-                 float *__restrict__ send_s, int32_t *__restrict__ send_tok) {
-    const int lane = threadIdx.x & 31;
-    const int cpr = H >> 4;  // 16-element chunks per row
-    const int Sb = H >> 7;
+// ------------------------------------------------------------ quant + pack
+//
+// One CTA works through (token, piece) items, a piece being up to
+// kPieceElems elements of the row (a multiple of 128, so no scale block
+// straddles two pieces).  Per item: the bf16 piece arrives in shared memory
+// by one bulk copy (issued one item ahead, completion on an mbarrier); the
+// threads quantise it, 16 elements per thread and 8 threads per 128-element
+// block (amax by xor-shuffles within the group, scale = amax/448 and
+// q = e4m3_satfinite_rn(x/scale) with IEEE fp32 divisions), into an fp8
+// piece and its scales in shared memory; one thread then sends that piece
+// to each of the token's R send rows with R bulk stores (plus R bulk stores
+// of the scales).  Two buffers of each kind let the load of item n+1 and
+// the stores of item n-1 overlap the arithmetic of item n.
+constexpr int kPieceElems = 8192;
+
+__device__ __forceinline__ uint4 quant16(const uint4 &a, const uint4 &b, float scale) {
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const float f0 = bf16_lo(w[2 * u]), f1 = bf16_hi(w[2 * u]);
+        const float f2 = bf16_lo(w[2 * u + 1]), f3 = bf16_hi(w[2 * u + 1]);
+        const uint32_t lo = cvt_pair(__fdiv_rn(f0, scale), __fdiv_rn(f1, scale));
+        const uint32_t hi = cvt_pair(__fdiv_rn(f2, scale), __fdiv_rn(f3, scale));
+        o[u] = lo | (hi << 16);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ float amax16(const uint4 &a, const uint4 &b) {
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    float m = 0.0f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[u])), fabsf(bf16_hi(w[u]))));
+    return m;
+}
+
+__global__ void __launch_bounds__(256)
+    k_quant_pack_staged(int T, int R, int H, int P, long long tok0, long long nitems,
+                        const uint16_t *__restrict__ x, const int32_t *__restrict__ slot_row,
+                        uint8_t *__restrict__ send_q, float *__restrict__ send_s,
+                        int32_t *__restrict__ send_tok, int32_t *__restrict__ status) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    unsigned char *sm = align128(smem_raw);
+    uint16_t *xbuf = reinterpret_cast<uint16_t *>(sm);            // [2][P] bf16
+    uint8_t *qbuf = sm + (size_t)4 * P;                           // [2][P] fp8
+    float *sbuf = reinterpret_cast<float *>(sm + (size_t)6 * P);  // [2][P/128]
+    __shared__ uint64_t xbar[2];
+    __shared__ long long rows[2][MOE_MAX_TOPK];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthr = blockDim.x;
+    const int Sb = H >> 7, npieces = (H + P - 1) / P;
     const long long TR = (long long)T * R;
-    const long long stride = (long long)gridDim.x * blockDim.x;
-    for (long long c0 = (long long)blockIdx.x * blockDim.x + (threadIdx.x & ~31); c0 < nchunks;
-         c0 += stride) {
-        const long long c = c0 + lane;
-        const bool in = c < nchunks;
-        const long long tok = in ? c / cpr : 0;
-        const int part = in ? (int)(c - tok * cpr) : 0;
-        uint4 a = make_uint4(0, 0, 0, 0), b = a;
-        if (in) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(x + tok * H + (long long)part * 16);
-            a = __ldcs(src);
-            b = __ldcs(src + 1);
+    const bool bulk_scales = (Sb & 3) == 0;
+
+    if (tid == 0) {
+        mbar_init(&xbar[0], 1);
+        mbar_init(&xbar[1], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    auto issue_load = [&](long long item, int b) {
+        const long long tok = tok0 + div_nonneg(item, npieces);
+        const int off = (int)(item - div_nonneg(item, npieces) * npieces) * P;
+        const int len = min(P, H - off);
+        mbar_arrive_expect_tx(&xbar[b], (uint32_t)len * 2u);
+        bulk_g2s(xbuf + (size_t)b * P, x + tok * H + off, (uint32_t)len * 2u, &xbar[b]);
+    };
+
+    const long long first = blockIdx.x, G = gridDim.x;
+    if (tid == 0 && first < nitems) issue_load(first, 0);
+    bool timed_out = false;
+    // thread tid < R: the slot of the current item, read one item ahead
+    int pref = -1;
+    if (tid < R && first < nitems)
+        pref = __ldg(slot_row + (tok0 + div_nonneg(first, npieces)) * R + tid);
+
+    int n = 0;
+    for (long long item = first; item < nitems; item += G, ++n) {
+        const int b = n & 1;
+        const long long tok = tok0 + div_nonneg(item, npieces);
+        const int piece = (int)(item - (tok - tok0) * npieces);
+        const int off = piece * P, len = min(P, H - off), nch = len >> 4;
+        const long long s = div_nonneg(tok, T);
+        const int t = (int)(tok - s * T);
+        if (tid == 0 && item + G < nitems) issue_load(item + G, b ^ 1);
+        if (tid == 0) bulk_wait_read<1>();  // stores of item n-2 are done with buffer b
+        const bool ok = mbar_wait(&xbar[b], (uint32_t)((n >> 1) & 1));
+        if (__syncthreads_or(!ok)) {
+            timed_out = true;
+            break;
         }
-        float f[16];
-        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            f[2 * u] = bf16_lo(w[u]);
-            f[2 * u + 1] = bf16_hi(w[u]);
-        }
-        float amax = 0.0f;
-#pragma unroll
-        for (int u = 0; u < 16; ++u) amax = fmaxf(amax, fabsf(f[u]));
-        amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
-        amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4));
-        const float scale = __fdiv_rn(amax, 448.0f);
-        uint4 q = make_uint4(0, 0, 0, 0);
-        if (amax > 0.0f) {
-            uint32_t o[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const uint32_t lo = cvt_pair(__fdiv_rn(f[4 * u], scale), __fdiv_rn(f[4 * u + 1], scale));
-                const uint32_t hi =
-                    cvt_pair(__fdiv_rn(f[4 * u + 2], scale), __fdiv_rn(f[4 * u + 3], scale));
-                o[u] = lo | (hi << 16);
+
+        const uint16_t *xs = xbuf + (size_t)b * P;
+        uint8_t *qs = qbuf + (size_t)b * P;
+        float *ss = sbuf + (size_t)b * (P >> 7);
+        for (int cb = warp * 32; cb < nch; cb += nthr) {
+            const int c = cb + lane;
+            const bool in = c < nch;
+            uint4 va = make_uint4(0, 0, 0, 0), vb = va;
+            if (in) {
+                const uint4 *p = reinterpret_cast<const uint4 *>(xs + (size_t)c * 16);
+                va = p[0];
+                vb = p[1];
             }
-            q = make_uint4(o[0], o[1], o[2], o[3]);
+            float amax = amax16(va, vb);
+            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4));
+            const float scale = __fdiv_rn(amax, 448.0f);
+            const uint4 q = amax > 0.0f ? quant16(va, vb, scale) : make_uint4(0, 0, 0, 0);
+            if (in) {
+                reinterpret_cast<uint4 *>(qs)[c] = q;
+                if ((c & 7) == 0) ss[c >> 3] = scale;
+            }
         }
-        if (in) {
-            const long long s = tok / T;
-            const int t = (int)(tok - s * T);
-            const int32_t *sl = slot_row + tok * R;
+        fence_proxy_async_smem();
+        if (tid < R) rows[b][tid] = (pref >= 0 && pref < TR) ? s * TR + pref : -1;
+        __syncthreads();
+        if (tid < R && item + G < nitems)
+            pref = __ldg(slot_row + (tok0 + div_nonneg(item + G, npieces)) * R + tid);
+        if (tid == 0) {
             for (int k = 0; k < R; ++k) {
-                const int sr = __ldg(sl + k);
-                if (sr < 0 || sr >= TR) continue;  // skipped assignment
-                const long long row = s * TR + sr;
-                *reinterpret_cast<uint4 *>(send_q + row * H + (long long)part * 16) = q;
-                if ((part & 7) == 0) send_s[row * Sb + (part >> 3)] = scale;
-                if (part == 0) send_tok[row] = t;
+                const long long row = rows[b][k];
+                if (row < 0) continue;
+                bulk_s2g(send_q + row * H + off, qs, (uint32_t)len);
+                if (bulk_scales)
+                    bulk_s2g(send_s + row * Sb + (off >> 7), ss, (uint32_t)(len >> 7) * 4u);
             }
+            bulk_commit();
+        }
+        if (!bulk_scales) {
+            const int nb = len >> 7;
+            for (int i = tid; i < R * nb; i += nthr) {
+                const long long row = rows[b][i / nb];
+                if (row >= 0) send_s[row * Sb + (off >> 7) + i % nb] = ss[i % nb];
+            }
+        }
+        if (piece == 0 && tid < R && rows[b][tid] >= 0) send_tok[rows[b][tid]] = t;
+    }
+    if (tid == 0) {
+        bulk_wait_all();
+        if (timed_out) {
+            flag(status, MOE_ST_TIMEOUT);
+            // let the loads of items n and n+1 land before shared memory goes away
+            mbar_wait(&xbar[n & 1], (uint32_t)((n >> 1) & 1));
+            if (first + (long long)(n + 1) * G < nitems)
+                mbar_wait(&xbar[(n + 1) & 1], (uint32_t)(((n + 1) >> 1) & 1));
         }
     }
 }
 
+static int quant_threads(int nch) {
+    // a block size that divides the piece's 16-element chunks into whole passes
+    for (int w = 8; w >= 1; --w)
+        if (nch % (32 * w) == 0) return 32 * w;
+    return nch >= 256 ? 256 : 32 * ((nch + 31) / 32);
+}
+
 cudaError_t launch_quant_pack(const moe_shape &sh, const uint16_t *x, const int32_t *slot_row,
-                              uint8_t *send_q, float *send_s, int32_t *send_tok, cudaStream_t st) {
-    const long long nchunks = (long long)sh.N * sh.T * (sh.H / 16);
-    if (nchunks == 0) return cudaSuccess;
-    const long long need = (nchunks + kQuantThreads - 1) / kQuantThreads;
-    const long long cap_blocks = (long long)sm_count() * (2048 / kQuantThreads);
-    const int grid = (int)(need < cap_blocks ? need : cap_blocks);
-    k_quant_pack<<<grid, kQuantThreads, 0, st>>>(sh.T, sh.R, sh.H, nchunks, x, slot_row, send_q,
-                                                 send_s, send_tok);
-    return cudaGetLastError();
+                              uint8_t *send_q, float *send_s, int32_t *send_tok, int32_t *status,
+                              cudaStream_t st, long long tok0, long long tok1) {
+    if (tok1 < 0) tok1 = (long long)sh.N * sh.T;
+    const long long ntok = tok1 - tok0;
+    if (ntok <= 0) return cudaSuccess;
+    const int P = sh.H < kPieceElems ? sh.H : kPieceElems;
+    const long long nitems = ntok * ((sh.H + P - 1) / P);
+    const int threads = quant_threads(P / 16);
+    const int smem = 6 * P + (P / 128) * 8 + 128;
+    static int cached_dev = -1, cached_smem = -1, cached_threads = -1, cached_occ = 1;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev != cached_dev || smem != cached_smem || threads != cached_threads) {
+        err = cudaFuncSetAttribute(k_quant_pack_staged, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   smem);
+        if (err != cudaSuccess) return err;
+        int occ = 0;
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_quant_pack_staged, threads, smem);
+        if (err != cudaSuccess) return err;
+        cached_occ = occ < 1 ? 1 : occ;
+        cached_dev = dev;
+        cached_smem = smem;
+        cached_threads = threads;
+    }
+    long long grid = (long long)sm_count() * cached_occ;
+    if (grid > nitems) grid = nitems;
+    return launch_kernel(k_quant_pack_staged, dim3((unsigned)grid), dim3(threads), (size_t)smem,
+                         st, sh.T, sh.R, sh.H, P, tok0, nitems, x, slot_row, send_q, send_s,
+                         send_tok, status);
 }
 
 }  // namespace moe

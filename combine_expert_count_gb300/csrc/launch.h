@@ -13,28 +13,37 @@ cudaError_t launch_route_count(const moe_shape &sh, const int32_t *idx, int32_t 
                                int32_t *send_off, int32_t *eso, int32_t *slot_row,
                                int32_t *status, cudaStream_t st);
 
+cudaError_t launch_route(const moe_shape &sh, int cap, const int32_t *idx, int32_t *cnt,
+                         int32_t *send_off, int32_t *eso, int32_t *slot_row, int32_t *grp_off,
+                         int32_t *seg_off, int32_t *csend_off, int32_t *m_sizes, int32_t *status,
+                         cudaStream_t st);
+
 cudaError_t launch_exchange(const moe_shape &sh, int cap, const int32_t *cnt,
                             const int32_t *send_off, int32_t *grp_off, int32_t *seg_off,
                             int32_t *csend_off, int32_t *m_sizes, int32_t *status,
                             cudaStream_t st);
 
 cudaError_t launch_quant_pack(const moe_shape &sh, const uint16_t *x, const int32_t *slot_row,
-                              uint8_t *send_q, float *send_s, int32_t *send_tok, cudaStream_t st);
+                              uint8_t *send_q, float *send_s, int32_t *send_tok, int32_t *status,
+                              cudaStream_t st, long long tok0 = 0, long long tok1 = -1);
 
 cudaError_t launch_dispatch_pull(const moe_shape &sh, int cap, const uint8_t *send_q,
                                  const float *send_s, const int32_t *send_tok,
                                  const int32_t *eso, const int32_t *seg_off, uint8_t *grp_q,
-                                 float *grp_s, int32_t *grp_src, int32_t *status, cudaStream_t st);
+                                 float *grp_s, int32_t *grp_src, int32_t *status, cudaStream_t st,
+                                 long long row0 = 0, long long row1 = -1);
 
 cudaError_t launch_combine_pack(const moe_shape &sh, int cap, const uint16_t *y,
                                 const int32_t *eso, const int32_t *send_off,
                                 const int32_t *seg_off, const int32_t *csend_off, uint16_t *csend,
-                                int32_t *status, cudaStream_t st);
+                                int32_t *status, cudaStream_t st, long long row0 = 0,
+                                long long row1 = -1);
 
 cudaError_t launch_combine_reduce(const moe_shape &sh, int cap, const uint16_t *csend,
                                   const int32_t *idx, const float *w, const int32_t *slot_row,
                                   const int32_t *send_off, const int32_t *csend_off,
-                                  uint16_t *out, cudaStream_t st);
+                                  uint16_t *out, cudaStream_t st, long long tok0 = 0,
+                                  long long tok1 = -1);
 
 cudaError_t launch_expert_standin(const moe_shape &sh, int cap, int mode, const uint8_t *grp_q,
                                   const float *grp_s, const int32_t *grp_off, uint16_t *y,

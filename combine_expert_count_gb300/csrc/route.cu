@@ -21,12 +21,15 @@ namespace moe {
 
 constexpr int kRouteThreads = 1024;
 
-__global__ void __launch_bounds__(kRouteThreads, 1)
-    k_route_count(int N, int T, int E, int R, const int32_t *__restrict__ idx,
-                  int32_t *__restrict__ cnt_out, int32_t *__restrict__ send_off,
-                  int32_t *__restrict__ eso_out, int32_t *__restrict__ slot_row,
-                  int32_t *__restrict__ status) {
-    extern __shared__ int smem[];
+// Sender role of rank s = blockIdx.x: counts, scans and stable slots.
+// `smem` holds 4*E ints and an E x 32 u16 table.
+__device__ __forceinline__ void route_sender(int N, int T, int E, int R,
+                                             const int32_t *__restrict__ idx,
+                                             int32_t *__restrict__ cnt_out,
+                                             int32_t *__restrict__ send_off,
+                                             int32_t *__restrict__ eso_out,
+                                             int32_t *__restrict__ slot_row,
+                                             int32_t *__restrict__ status, int *smem) {
     int *cnt = smem;           // [E] counts
     int *base = cnt + E;       // [E] exclusive scan of counts
     int *run = base + E;       // [E] assignments seen in earlier chunks
@@ -34,6 +37,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     unsigned short *tab = reinterpret_cast<unsigned short *>(ctot + E);  // [E][32]
     __shared__ int wsum[32];
     __shared__ int total;
+    __syncthreads();  // callers may reuse shared memory around this
 
     const int s = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nw = blockDim.x >> 5;
@@ -98,19 +102,28 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     }
 }
 
-__global__ void __launch_bounds__(1024)
-    k_exchange(int N, int E, int cap, const int32_t *__restrict__ cnt,
-               const int32_t *__restrict__ send_off, int32_t *__restrict__ grp_off,
-               int32_t *__restrict__ seg_off, int32_t *__restrict__ csend_off,
-               int32_t *__restrict__ m_sizes, int32_t *__restrict__ status) {
+__global__ void __launch_bounds__(kRouteThreads, 1)
+    k_route_count(int N, int T, int E, int R, const int32_t *__restrict__ idx,
+                  int32_t *__restrict__ cnt_out, int32_t *__restrict__ send_off,
+                  int32_t *__restrict__ eso_out, int32_t *__restrict__ slot_row,
+                  int32_t *__restrict__ status) {
+    extern __shared__ int smem[];
+    route_sender(N, T, E, R, idx, cnt_out, send_off, eso_out, slot_row, status, smem);
+}
+
+// Receiver role of rank r = blockIdx.x given v = the count of run f = j*N + s
+// (local expert j, sender s) for tid < F = Er*N, and w = the rows sender
+// tid sends to r for tid < N.
+__device__ __forceinline__ void route_receiver(int N, int E, int cap, int v, int w,
+                                               int32_t *__restrict__ grp_off,
+                                               int32_t *__restrict__ seg_off,
+                                               int32_t *__restrict__ csend_off,
+                                               int32_t *__restrict__ m_sizes,
+                                               int32_t *__restrict__ status) {
     __shared__ int wsum[32];
     __shared__ int total;
     __shared__ int excl[MOE_MAX_EXPERTS + 1];
     const int r = blockIdx.x, tid = threadIdx.x, Er = E / N, F = Er * N;
-
-    // runs in (local expert j, sender s) order: f = j*N + s
-    const int j = tid / N, s = tid - (tid / N) * N;
-    const int v = tid < F ? __ldg(cnt + (size_t)s * E + r * Er + j) : 0;
     const int incl = block_inclusive_scan(v, wsum, &total);
     if (tid < F) {
         excl[tid] = incl - v;
@@ -122,14 +135,86 @@ __global__ void __launch_bounds__(1024)
     if (tid <= Er) grp_off[(size_t)r * (Er + 1) + tid] = excl[tid * N];
     if (tid < Er) m_sizes[(size_t)r * Er + tid] = excl[(tid + 1) * N] - excl[tid * N];
     if (tid == 0 && recv > cap) flag(status, MOE_ST_CAPACITY);
-
-    // rows going back to each sender s, in sender order
-    const int w = tid < N ? __ldg(send_off + (size_t)tid * (N + 1) + r + 1) -
-                                __ldg(send_off + (size_t)tid * (N + 1) + r)
-                          : 0;
     const int wi = block_inclusive_scan(w, wsum, &total);
     if (tid < N) csend_off[(size_t)r * (N + 1) + tid] = wi - w;
     if (tid == 0) csend_off[(size_t)r * (N + 1) + N] = total;
+}
+
+__global__ void __launch_bounds__(1024)
+    k_exchange(int N, int E, int cap, const int32_t *__restrict__ cnt,
+               const int32_t *__restrict__ send_off, int32_t *__restrict__ grp_off,
+               int32_t *__restrict__ seg_off, int32_t *__restrict__ csend_off,
+               int32_t *__restrict__ m_sizes, int32_t *__restrict__ status) {
+    const int r = blockIdx.x, tid = threadIdx.x, Er = E / N, F = Er * N;
+    // runs in (local expert j, sender s) order: f = j*N + s
+    const int j = tid / N, s = tid - (tid / N) * N;
+    const int v = tid < F ? __ldg(cnt + (size_t)s * E + r * Er + j) : 0;
+    // rows going back to each sender, in sender order
+    const int w = tid < N ? __ldg(send_off + (size_t)tid * (N + 1) + r + 1) -
+                                __ldg(send_off + (size_t)tid * (N + 1) + r)
+                          : 0;
+    route_receiver(N, E, cap, v, w, grp_off, seg_off, csend_off, m_sizes, status);
+}
+
+// Rank that owns flat assignment index i.
+__device__ __forceinline__ int sender_of(long long i, long long TR) {
+    return (int)div_nonneg(i, TR);
+}
+
+// Both roles in one launch: block r is sender r (as k_route_count) and
+// receiver r.  The receiver needs every sender's count for its own Er
+// experts; rather than waiting for the other blocks it recounts them from all
+// ranks' ids (N*T*R ints, read from L2), so no block waits on another.
+__global__ void __launch_bounds__(kRouteThreads, 1)
+    k_route(int N, int T, int E, int R, int cap, const int32_t *__restrict__ idx,
+            int32_t *__restrict__ cnt_out, int32_t *__restrict__ send_off,
+            int32_t *__restrict__ eso_out, int32_t *__restrict__ slot_row,
+            int32_t *__restrict__ grp_off, int32_t *__restrict__ seg_off,
+            int32_t *__restrict__ csend_off, int32_t *__restrict__ m_sizes,
+            int32_t *__restrict__ status) {
+    extern __shared__ int smem[];
+    const int r = blockIdx.x, tid = threadIdx.x, Er = E / N, F = Er * N;
+    int *rc = smem;  // [N][Er] counts of (sender, local expert), then reused
+    for (int i = tid; i < F; i += blockDim.x) rc[i] = 0;
+    __syncthreads();
+    const long long all = (long long)N * T * R, TR = (long long)T * R;
+    const int lo = r * Er;
+    // four ids per 16-byte load, four loads in flight per thread
+    const long long n4 = all >> 2;
+    const int4 *id4 = reinterpret_cast<const int4 *>(idx);
+    for (long long i0 = tid; i0 < n4; i0 += 4LL * blockDim.x) {
+        int4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const long long i = i0 + (long long)u * blockDim.x;
+            v[u] = i < n4 ? __ldg(id4 + i) : make_int4(-1, -1, -1, -1);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const long long i = (i0 + (long long)u * blockDim.x) * 4;
+            const int e4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const unsigned j = (unsigned)(e4[q] - lo);
+                // only 1 in N ids land here: the sender's index is worked out then
+                if (j < (unsigned)Er) atomicAdd(&rc[sender_of(i + q, TR) * Er + (int)j], 1);
+            }
+        }
+    }
+    for (long long i = (n4 << 2) + tid; i < all; i += blockDim.x) {
+        const unsigned j = (unsigned)(__ldg(idx + i) - lo);
+        if (j < (unsigned)Er) atomicAdd(&rc[sender_of(i, TR) * Er + (int)j], 1);
+    }
+    __syncthreads();
+    int v = 0, w = 0;
+    if (tid < F) {
+        const int j = tid / N, s = tid - j * N;
+        v = rc[s * Er + j];
+    }
+    if (tid < N)
+        for (int j = 0; j < Er; ++j) w += rc[tid * Er + j];
+    route_receiver(N, E, cap, v, w, grp_off, seg_off, csend_off, m_sizes, status);
+    route_sender(N, T, E, R, idx, cnt_out, send_off, eso_out, slot_row, status, smem);
 }
 
 static size_t route_smem(int E) { return (size_t)E * 4 * sizeof(int) + (size_t)E * 32 * 2; }
@@ -153,6 +238,28 @@ cudaError_t launch_route_count(const moe_shape &sh, const int32_t *idx, int32_t 
     }
     k_route_count<<<sh.N, kRouteThreads, smem, st>>>(sh.N, sh.T, sh.E, sh.R, idx, cnt, send_off,
                                                      eso, slot_row, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_route(const moe_shape &sh, int cap, const int32_t *idx, int32_t *cnt,
+                         int32_t *send_off, int32_t *eso, int32_t *slot_row, int32_t *grp_off,
+                         int32_t *seg_off, int32_t *csend_off, int32_t *m_sizes, int32_t *status,
+                         cudaStream_t st) {
+    cudaError_t err = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
+    if (err != cudaSuccess) return err;
+    static int attr_dev = -1;
+    int dev = 0;
+    err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev != attr_dev) {
+        err = cudaFuncSetAttribute(k_route, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)route_smem(MOE_MAX_EXPERTS));
+        if (err != cudaSuccess) return err;
+        attr_dev = dev;
+    }
+    k_route<<<sh.N, kRouteThreads, route_smem(sh.E), st>>>(sh.N, sh.T, sh.E, sh.R, cap, idx, cnt,
+                                                         send_off, eso, slot_row, grp_off, seg_off,
+                                                         csend_off, m_sizes, status);
     return cudaGetLastError();
 }
 

@@ -29,9 +29,9 @@ _lib = None
 MOE_OK, MOE_EINVAL, MOE_ENOTSUP, MOE_ECUDA = 0, -1, -2, -3
 MOE_ST_BAD_EXPERT, MOE_ST_CAPACITY, MOE_ST_TIMEOUT = 1, 2, 4
 
-EXPORTS = ("moe_sizes_query", "moe_route_count", "moe_exchange", "moe_dispatch_send",
-           "moe_dispatch_recv", "moe_combine_send", "moe_combine_recv", "moe_expert_standin",
-           "moe_e4m3_encode", "moe_strerror", "moe_version")
+EXPORTS = ("moe_sizes_query", "moe_route_count", "moe_exchange", "moe_route", "moe_dispatch_send",
+           "moe_dispatch_recv", "moe_combine_send", "moe_combine_recv", "moe_dispatch",
+           "moe_combine", "moe_expert_standin", "moe_e4m3_encode", "moe_strerror", "moe_version")
 
 
 class moe_shape(ctypes.Structure):
@@ -47,6 +47,15 @@ _SIZE_FIELDS = ("cap", "send_rows", "bytes_x", "bytes_topk_idx", "bytes_expert_c
 
 class moe_sizes(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in _SIZE_FIELDS]
+
+
+_BUFFER_FIELDS = ("topk_idx", "topk_w", "x", "expert_count", "send_off", "expert_send_off",
+                  "slot_row", "grp_off", "seg_off", "csend_off", "m_sizes", "send_q", "send_s",
+                  "send_tok", "grp_q", "grp_s", "grp_src", "y", "csend", "out", "status")
+
+
+class moe_buffers(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in _BUFFER_FIELDS]
 
 
 class MoeError(RuntimeError):
@@ -73,6 +82,9 @@ def lib() -> ctypes.CDLL:
             h.moe_sizes_query.argtypes = [sp, P(moe_sizes)]
             h.moe_route_count.argtypes = [sp] + [V] * 6 + [V]
             h.moe_exchange.argtypes = [sp] + [V] * 7 + [V]
+            h.moe_route.argtypes = [sp] + [V] * 10 + [V]
+            h.moe_dispatch.argtypes = [sp, P(moe_buffers), I, V]
+            h.moe_combine.argtypes = [sp, P(moe_buffers), I, V]
             h.moe_dispatch_send.argtypes = [sp] + [V] * 6 + [V]
             h.moe_dispatch_recv.argtypes = [sp] + [V] * 10 + [V]
             h.moe_combine_send.argtypes = [sp] + [V] * 8 + [V]
@@ -165,6 +177,20 @@ def moe_exchange(shape, expert_count, send_off, grp_off, seg_off, csend_off, m_s
         "moe_exchange")
 
 
+def moe_route(shape, topk_idx, expert_count, send_off, expert_send_off, slot_row, grp_off,
+              seg_off, csend_off, m_sizes, status, stream=None) -> None:
+    sh, z = _as_shape(shape), sizes_query(shape)
+    _check(lib().moe_route(
+        ctypes.byref(sh), _p(topk_idx, z.bytes_topk_idx, "topk_idx"),
+        _p(expert_count, z.bytes_expert_count, "expert_count"),
+        _p(send_off, z.bytes_send_off, "send_off"),
+        _p(expert_send_off, z.bytes_expert_send_off, "expert_send_off"),
+        _p(slot_row, z.bytes_topk_idx, "slot_row"), _p(grp_off, z.bytes_grp_off, "grp_off"),
+        _p(seg_off, z.bytes_seg_off, "seg_off"), _p(csend_off, z.bytes_send_off, "csend_off"),
+        _p(m_sizes, z.bytes_m_sizes, "m_sizes"), _p(status, 4, "status"), _s(stream)),
+        "moe_route")
+
+
 def moe_dispatch_send(shape, x, slot_row, send_q, send_s, send_tok, status, stream=None) -> None:
     sh, z = _as_shape(shape), sizes_query(shape)
     _check(lib().moe_dispatch_send(
@@ -211,6 +237,49 @@ def moe_combine_recv(shape, csend, topk_idx, topk_w, slot_row, send_off, csend_o
         _p(csend_off, z.bytes_send_off, "csend_off"), _p(out, z.bytes_x, "out"),
         _p(status, 4, "status"), _s(stream)),
         "moe_combine_recv")
+
+
+_DISPATCH_NEEDS = {"topk_idx": "bytes_topk_idx", "x": "bytes_x",
+                   "expert_count": "bytes_expert_count", "send_off": "bytes_send_off",
+                   "expert_send_off": "bytes_expert_send_off", "slot_row": "bytes_topk_idx",
+                   "grp_off": "bytes_grp_off", "seg_off": "bytes_seg_off",
+                   "csend_off": "bytes_send_off", "m_sizes": "bytes_m_sizes",
+                   "send_q": "bytes_send_q", "send_s": "bytes_send_s",
+                   "send_tok": "bytes_send_tok", "grp_q": "bytes_grp_q", "grp_s": "bytes_grp_s",
+                   "grp_src": "bytes_grp_src"}
+_COMBINE_NEEDS = {"topk_idx": "bytes_topk_idx", "topk_w": "bytes_topk_idx", "y": "bytes_y",
+                  "expert_send_off": "bytes_expert_send_off", "send_off": "bytes_send_off",
+                  "slot_row": "bytes_topk_idx", "seg_off": "bytes_seg_off",
+                  "csend_off": "bytes_send_off", "csend": "bytes_y", "out": "bytes_x"}
+
+
+def _buffers(z: moe_sizes, tensors: dict, needs: dict) -> moe_buffers:
+    b = moe_buffers()
+    for name in _BUFFER_FIELDS:
+        t = tensors.get(name)
+        nbytes = 4 if name == "status" else getattr(z, needs[name]) if name in needs else 0
+        if name in needs or name == "status" or t is not None:
+            p = _p(t, nbytes, name)
+            setattr(b, name, p.value if p is not None else None)
+    return b
+
+
+def moe_dispatch(shape, tensors: dict, chunks: int = 0, stream=None) -> None:
+    """Whole dispatch in one call; ``tensors`` maps moe_buffers field names
+    (x, topk_idx, routing arrays, send and grouped buffers, status) to tensors."""
+    sh, z = _as_shape(shape), sizes_query(shape)
+    b = _buffers(z, tensors, _DISPATCH_NEEDS)
+    _check(lib().moe_dispatch(ctypes.byref(sh), ctypes.byref(b), int(chunks), _s(stream)),
+           "moe_dispatch")
+
+
+def moe_combine(shape, tensors: dict, chunks: int = 0, stream=None) -> None:
+    """Whole combine in one call; ``tensors`` as for moe_dispatch (y, topk_idx,
+    topk_w, routing arrays, csend, out, status)."""
+    sh, z = _as_shape(shape), sizes_query(shape)
+    b = _buffers(z, tensors, _COMBINE_NEEDS)
+    _check(lib().moe_combine(ctypes.byref(sh), ctypes.byref(b), int(chunks), _s(stream)),
+           "moe_combine")
 
 
 def moe_expert_standin(shape, mode: int, grp_q, grp_s, grp_off, y, stream=None) -> None:
@@ -270,15 +339,34 @@ class MoeBuffers:
         return sum(t.numel() * t.element_size() for t in vars(self).values()
                    if isinstance(t, torch.Tensor))
 
-    def route(self, topk_idx, stream=None) -> None:
+    def route(self, topk_idx, stream=None, fused: bool = True) -> None:
+        """Counts, offsets and slots: one ``moe_route`` launch, or
+        ``moe_route_count`` then ``moe_exchange`` with ``fused=False``."""
+        if fused:
+            moe_route(self.shape, topk_idx, self.expert_count, self.send_off,
+                      self.expert_send_off, self.slot_row, self.grp_off, self.seg_off,
+                      self.csend_off, self.m_sizes, self.status, stream)
+            return
         moe_route_count(self.shape, topk_idx, self.expert_count, self.send_off,
                         self.expert_send_off, self.slot_row, self.status, stream)
         moe_exchange(self.shape, self.expert_count, self.send_off, self.grp_off, self.seg_off,
                      self.csend_off, self.m_sizes, self.status, stream)
 
-    def dispatch(self, x, topk_idx, stream=None) -> None:
-        """route_count, exchange, dispatch_send, dispatch_recv."""
-        self.route(topk_idx, stream)
+    def tensors(self, **extra) -> dict:
+        """This object's buffers by moe_buffers field name, plus ``extra``."""
+        d = {n: getattr(self, n) for n in _BUFFER_FIELDS if hasattr(self, n)}
+        d.update(extra)
+        return d
+
+    def dispatch(self, x, topk_idx, stream=None, calls: str = "pipelined",
+                 chunks: int = 0) -> None:
+        """The dispatch half.  ``calls``: "pipelined" (one moe_dispatch call,
+        sender chunks through L2), "fused_route" (moe_route then the two
+        dispatch calls) or "separate" (the four calls of the pages' steps)."""
+        if calls == "pipelined":
+            moe_dispatch(self.shape, self.tensors(x=x, topk_idx=topk_idx), chunks, stream)
+            return
+        self.route(topk_idx, stream, calls == "fused_route")
         moe_dispatch_send(self.shape, x, self.slot_row, self.send_q, self.send_s, self.send_tok,
                           self.status, stream)
         moe_dispatch_recv(self.shape, self.send_q, self.send_s, self.send_tok, self.expert_count,
@@ -289,9 +377,17 @@ class MoeBuffers:
         """The grouped-GEMM stand-in (identity or per-expert scale)."""
         moe_expert_standin(self.shape, mode, self.grp_q, self.grp_s, self.grp_off, self.y, stream)
 
-    def combine(self, topk_idx, topk_w, y=None, out=None, stream=None) -> torch.Tensor:
-        """combine_send, combine_recv; returns ``out``."""
+    def combine(self, topk_idx, topk_w, y=None, out=None, stream=None, calls: str = "pipelined",
+                chunks: int = 0) -> torch.Tensor:
+        """The combine half; returns ``out``.  ``calls``: "pipelined" (one
+        moe_combine call) or anything else for moe_combine_send then
+        moe_combine_recv."""
         out = self.out if out is None else out
+        if calls == "pipelined":
+            moe_combine(self.shape, self.tensors(topk_idx=topk_idx, topk_w=topk_w,
+                                                 y=self.y if y is None else y, out=out),
+                        chunks, stream)
+            return out
         moe_combine_send(self.shape, self.y if y is None else y, self.expert_count,
                          self.expert_send_off, self.send_off, self.seg_off, self.csend_off,
                          self.csend, self.status, stream)

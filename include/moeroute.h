@@ -154,6 +154,18 @@ int moe_exchange(const moe_shape *shape, const int32_t *expert_count, const int3
                  int32_t *grp_off, int32_t *seg_off, int32_t *csend_off, int32_t *m_sizes,
                  int32_t *status, void *stream);
 
+/* moe_route_count and moe_exchange in one launch (same outputs, same status
+ * bits, *status cleared first).  Block r plays sender r, as in
+ * moe_route_count, and receiver r, as in moe_exchange; instead of waiting for
+ * the other senders' counts it recounts, from all ranks' topk_idx, the
+ * assignments that land on its own experts.  The pages exchange counts
+ * between ranks first ("Send and receive buffers"); on one GPU every rank's
+ * ids are already in memory, so no rank has to wait for another. */
+int moe_route(const moe_shape *shape, const int32_t *topk_idx, int32_t *expert_count,
+              int32_t *send_off, int32_t *expert_send_off, int32_t *slot_row, int32_t *grp_off,
+              int32_t *seg_off, int32_t *csend_off, int32_t *m_sizes, int32_t *status,
+              void *stream);
+
 /* Dispatch send, step 2: block-scaled fp8 quantisation fused with the pack
  * ("Dispatch and combine"; "Evaluation": block-scaled fp8 dispatch).  Per
  * token and 128-element block: amax = max|x|, scale = amax/448 (fp32
@@ -217,6 +229,49 @@ int moe_expert_standin(const moe_shape *shape, int mode, const uint8_t *grp_q,
  * saturate to +-448), element-wise over n values; exposed so the encoder can
  * be compared with other implementations. */
 int moe_e4m3_encode(const float *v, uint8_t *out, int64_t n, void *stream);
+
+/* ---------------------------------------------------------------- pipelined
+ * The whole dispatch and the whole combine as one call each.  Outputs are
+ * exactly those of the separate calls above (route + dispatch_send +
+ * dispatch_recv; combine_send + combine_recv).  Optionally the senders are
+ * taken in chunks of consecutive ranks, each chunk's producer followed by its
+ * consumer so the consumer reads rows the producer just left in L2. */
+typedef struct {
+    const int32_t *topk_idx;   /* [N][T][R] */
+    const float *topk_w;       /* [N][T][R] (combine) */
+    const uint16_t *x;         /* [N][T][H] bf16 (dispatch) */
+    int32_t *expert_count;     /* [N][E] */
+    int32_t *send_off;         /* [N][N+1] */
+    int32_t *expert_send_off;  /* [N][E+1] */
+    int32_t *slot_row;         /* [N][T][R] */
+    int32_t *grp_off;          /* [N][Er+1] */
+    int32_t *seg_off;          /* [N][Er][N] */
+    int32_t *csend_off;        /* [N][N+1] */
+    int32_t *m_sizes;          /* [N][Er] */
+    uint8_t *send_q;           /* [N][T*R][H] */
+    float *send_s;             /* [N][T*R][H/128] */
+    int32_t *send_tok;         /* [N][T*R] */
+    uint8_t *grp_q;            /* [N][cap][H] */
+    float *grp_s;              /* [N][cap][H/128] */
+    int32_t *grp_src;          /* [N][cap][2] */
+    const uint16_t *y;         /* [N][cap][H] bf16 expert outputs (combine) */
+    uint16_t *csend;           /* [N][cap][H] */
+    uint16_t *out;             /* [N][T][H] bf16 (combine) */
+    int32_t *status;           /* one int32 */
+} moe_buffers;
+
+/* moe_route, then for each chunk of senders: moe_dispatch_send of the
+ * chunk's tokens, moe_dispatch_recv of the chunk's send rows.  Uses x,
+ * topk_idx, the routing arrays, the send buffers and the grouped buffers.
+ * chunks = 0 or 1: no chunking; chunks > 1 splits the N ranks into that many
+ * near-equal chunks. */
+int moe_dispatch(const moe_shape *shape, const moe_buffers *b, int chunks, void *stream);
+
+/* For each chunk of destination ranks: moe_combine_send of the rows going
+ * back to them, then moe_combine_recv of their tokens.  Uses y, topk_idx,
+ * topk_w, the routing arrays, csend and out; the routing arrays must come
+ * from a dispatch of the same topk_idx.  chunks as for moe_dispatch. */
+int moe_combine(const moe_shape *shape, const moe_buffers *b, int chunks, void *stream);
 
 /* Static description of an error code or status bit set. */
 const char *moe_strerror(int code);

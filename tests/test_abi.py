@@ -98,7 +98,7 @@ def test_null_and_misaligned_pointers_rejected(lib):
     L = m.lib()
     # every pointer slot of every entry point, one at a time
     calls = {
-        "moe_route_count": 6, "moe_exchange": 7, "moe_dispatch_send": 6,
+        "moe_route_count": 6, "moe_exchange": 7, "moe_route": 10, "moe_dispatch_send": 6,
         "moe_dispatch_recv": 10, "moe_combine_send": 8, "moe_combine_recv": 8,
     }
     for name, nptr in calls.items():
@@ -108,6 +108,15 @@ def test_null_and_misaligned_pointers_rejected(lib):
                 args = [good] * nptr
                 args[i] = p
                 assert fn(ctypes.byref(sh), *args, None) == m.MOE_EINVAL, (name, i, p)
+    for fn in (L.moe_dispatch, L.moe_combine):
+        assert fn(ctypes.byref(sh), None, 0, None) == m.MOE_EINVAL
+        needs = m._DISPATCH_NEEDS if fn is L.moe_dispatch else m._COMBINE_NEEDS
+        for field in list(needs) + ["status"]:
+            b = m.moe_buffers(*([0x10000] * len(m._BUFFER_FIELDS)))
+            setattr(b, field, 0x10004)
+            assert fn(ctypes.byref(sh), ctypes.byref(b), 0, None) == m.MOE_EINVAL, field
+        b = m.moe_buffers(*([0x10000] * len(m._BUFFER_FIELDS)))
+        assert fn(ctypes.byref(sh), ctypes.byref(b), -1, None) == m.MOE_EINVAL
     assert L.moe_expert_standin(ctypes.byref(sh), 2, good, good, good, good, None) == m.MOE_EINVAL
     assert L.moe_expert_standin(ctypes.byref(sh), 0, bad, good, good, good, None) == m.MOE_EINVAL
     assert L.moe_e4m3_encode(null, good, 4, None) == m.MOE_EINVAL

@@ -55,6 +55,27 @@ def test_config_full_parity(name):
     G.compare_with_oracle(w, buf, o)
 
 
+@pytest.mark.parametrize("calls", ["separate", "fused_route"])
+@pytest.mark.parametrize("name", ["tiny", "dsv3_decode", "kimi_k2_decode", "qwen3_skew"])
+def test_other_call_forms(name, calls):
+    """The per-step calls (moe_route_count, moe_exchange, moe_dispatch_send,
+    moe_dispatch_recv, moe_combine_send, moe_combine_recv), and the same with
+    moe_route, give the oracle's outputs like the pipelined calls."""
+    w = W.CONFIGS[name]
+    d = W.generate(w)
+    buf = G.run_path(w, G.to_dev(d), calls=calls)
+    G.compare_with_oracle(w, buf, _oracle(w, d, _exact_cap(w, d)))
+
+
+@pytest.mark.parametrize("chunks", [1, 2, 3, 5, 16])
+def test_pipeline_chunk_counts(chunks):
+    """Every chunking of the sender ranks gives the same outputs."""
+    w = W.CONFIGS["dsv3_decode"].replace(T=32)
+    d = W.generate(w)
+    buf = G.run_path(w, G.to_dev(d), chunks=chunks)
+    G.compare_with_oracle(w, buf, _oracle(w, d, _exact_cap(w, d)))
+
+
 def test_worst_case_reduced_t_full_parity():
     """All tokens routed to rank 0's experts, compared in full."""
     w = W.CONFIGS["qwen3_worst"].replace(T=64)
@@ -125,8 +146,12 @@ def _grid():
 def test_small_shape_grid(N, T, E, R, H):
     w = W.Workload("grid", N=N, T=T, H=H, E=E, R=R, seed=7 + N * 1000 + T * 100 + E * 10 + R)
     d = W.generate(w)
-    buf = G.run_path(w, G.to_dev(d))
-    G.compare_with_oracle(w, buf, _oracle(w, d, w.default_cap))
+    o = _oracle(w, d, w.default_cap)
+    for calls in ("pipelined", "separate", "fused_route"):
+        buf = G.run_path(w, G.to_dev(d), calls=calls, chunks=0 if calls == "pipelined" else 1)
+        G.compare_with_oracle(w, buf, o)
+    buf = G.run_path(w, G.to_dev(d), chunks=N)
+    G.compare_with_oracle(w, buf, o)
 
 
 def test_empty_batch():
@@ -149,13 +174,14 @@ def test_empty_batch():
     assert np.all(G.host(buf.grp_off) == 0) and np.all(G.host(buf.csend_off) == 0)
 
 
-def test_bad_expert_ids_are_skipped_and_flagged():
+@pytest.mark.parametrize("calls", ["pipelined", "separate", "fused_route"])
+def test_bad_expert_ids_are_skipped_and_flagged(calls):
     w = W.Workload("bad", N=2, T=8, H=256, E=8, R=2, seed=3)
     d = W.generate(w)
     d["topk_idx"][0, 1, 1] = -1
     d["topk_idx"][1, 5, 0] = 8
     d["topk_idx"][1, 6, 1] = 1 << 30
-    buf = G.run_path(w, G.to_dev(d))
+    buf = G.run_path(w, G.to_dev(d), calls=calls)
     o = _oracle(w, d, w.default_cap)
     assert o["status"] == ref.ST_BAD_EXPERT
     G.compare_with_oracle(w, buf, o)
@@ -163,10 +189,11 @@ def test_bad_expert_ids_are_skipped_and_flagged():
 
 
 @pytest.mark.parametrize("cap", [1, 7, 20])
-def test_capacity_overflow_drops_and_flags(cap):
+@pytest.mark.parametrize("calls", ["pipelined", "separate", "fused_route"])
+def test_capacity_overflow_drops_and_flags(cap, calls):
     w = W.Workload("cap", N=2, T=16, H=256, E=4, R=2, seed=11)
     d = W.generate(w)
-    buf = G.run_path(w, G.to_dev(d), cap=cap)
+    buf = G.run_path(w, G.to_dev(d), cap=cap, calls=calls, chunks=2)
     o = _oracle(w, d, cap)
     assert o["status"] & ref.ST_CAPACITY
     G.compare_with_oracle(w, buf, o)
@@ -214,6 +241,8 @@ def test_repeat_and_graph_replay_are_identical():
     with torch.cuda.graph(g, stream=s):
         b3.dispatch(dd["x"], dd["topk_idx"])
         b3.combine(dd["topk_idx"], dd["topk_w"])
+        b3.dispatch(dd["x"], dd["topk_idx"], calls="separate")
+        b3.combine(dd["topk_idx"], dd["topk_w"], calls="separate")
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(b3.out, b1.out)
