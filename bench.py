@@ -1,21 +1,20 @@
 #!/usr/bin/env python3
 """Dispatch + combine benchmark on one GB300.
 
-One step = one MoE layer's hot path over one batch: route (route_count and
-exchange in one launch), dispatch_send, dispatch_recv (dispatch) and
-combine_send, combine_recv (combine), run through libmoeroute's C ABI as the
-two pipelined calls moe_dispatch and moe_combine (the same kernels, ordered
-by chunks of sender ranks so each consumer reads its producer's rows from
-L2); a second pass times the separate calls one by one for the per-kernel
-breakdown.  The grouped-GEMM
-stand-in runs once before timing (its output is the same every step) and is
-not timed.  Inputs are resident in HBM when timing starts; L2 is flushed
-(512 MiB write) before every step, outside the timed window.
+One step = one MoE layer's hot path over one batch, through libmoeroute's C
+ABI: moe_dispatch (route_count + exchange in one launch, then quantise +
+pack + receive shuffle in one launch) and moe_combine (combine send +
+receive in one launch).  Every output of the six separate calls of the
+pages' steps is written each step; a second timing runs those separate
+calls one by one.  The grouped-GEMM stand-in runs once before timing (its
+output is the same every step) and is not timed.  Inputs are resident in HBM
+when timing starts; L2 is flushed (512 MiB write) before every step, outside
+the timed window.
 
 Prints one JSON line: value = dispatch + combine microseconds per layer
-(lower is better), plus achieved HBM GB/s over the algorithmic bytes, the
-roofline of the dominant kernel, an end-to-end figure with host buffers, and
-the CPU oracle timed on a bounded sample as a baseline.
+(lower is better), achieved HBM GB/s over the bytes the timed calls must
+move, the roofline of the dominant kernel, an end-to-end figure with host
+buffers, and the CPU oracle timed on a bounded sample as a baseline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
   python bench.py --impl reference ...   (the CPU oracle as the reference arm)
@@ -43,31 +42,44 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 512 << 20
 KERNELS = ("route", "dispatch_send", "dispatch_recv", "combine_send", "combine_recv")
+FUSED = ("route", "dispatch_fused", "combine_fused")
 KERNEL_SYMBOL = {"route": "k_route (route_count + exchange)",
-                 "dispatch_send": "k_quant_pack", "dispatch_recv": "k_row_shuffle<DispatchMap>",
-                 "combine_send": "k_row_shuffle<CombineMap>", "combine_recv": "k_combine_reduce"}
+                 "dispatch_send": "k_quant_pack_staged<false>",
+                 "dispatch_recv": "k_row_copy<DispatchMap>",
+                 "combine_send": "k_row_copy<CombineMap>", "combine_recv": "k_combine_reduce",
+                 "dispatch_fused": "k_quant_pack_staged<true> (quantise + pack + receive shuffle)",
+                 "combine_fused": "k_combine_fused (combine send + receive)"}
 
 
 # ----------------------------------------------------------------- bytes
 
 
 def algorithmic_bytes(w, A: int) -> dict:
-    """Bytes each step must move, every materialised buffer written once and
-    read once; A = (token, expert) assignments routed.  Row_fp8 = H + 4*Sb."""
+    """Bytes per step, A = (token, expert) assignments routed, Row_fp8 =
+    H + 4*H/128.  "s8d": every materialised buffer written once and read
+    once (the separate calls move exactly this).  "fused": every buffer the
+    fused calls read or write, once -- the same outputs without re-reading
+    the send buffer and the combine send buffer."""
     N, T, H, R = w.N, w.T, w.H, w.R
     Sb = H // 128
     row8 = H + 4 * Sb
     x = 2 * N * T * H
-    per = {
-        "dispatch_send": x + A * (row8 + 4) + 4 * A,           # read x, slots; write rows+tok
-        "dispatch_recv": A * (row8 + 4) + A * (row8 + 8),      # read rows+tok; write rows+src
+    ids = 4 * N * T * R
+    separate = {
+        "route": 2 * ids,                                       # read ids, write slots
+        "dispatch_send": x + A * (row8 + 4) + 4 * A,            # read x, slots; write rows+tok
+        "dispatch_recv": A * (row8 + 4) + A * (row8 + 8),       # read rows+tok; write rows+src
         "combine_send": 2 * A * 2 * H,                          # read y rows; write csend rows
         "combine_recv": A * 2 * H + x + 12 * A,                 # read rows, idx/w/slot; write out
     }
-    dispatch = x + 3 * A * row8 + 8 * A
-    combine = 3 * A * 2 * H + x + 8 * A
-    return {"per_kernel": per, "dispatch": dispatch, "combine": combine,
-            "total": dispatch + combine}
+    fused = {
+        "route": 2 * ids,
+        "dispatch_fused": x + 2 * A * row8 + 8 * A + 4 * A + 8 * A,  # x, ids+slots; rows, tok, src
+        "combine_fused": 2 * A * 2 * H + x + 12 * A,            # y rows; csend rows, out; idx/w/slot
+    }
+    return {"separate": separate, "fused": fused,
+            "s8d_dispatch": x + 3 * A * row8 + 8 * A,
+            "s8d_combine": 3 * A * 2 * H + x + 8 * A}
 
 
 def measured_peak():
@@ -307,14 +319,13 @@ def run_ours(args) -> None:
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     tens = buf.tensors(x=x, topk_idx=idx, topk_w=wt)
-    pipelined = (
-        lambda: m.moe_dispatch(sh, tens, args.chunks),
-        lambda: m.moe_combine(sh, tens, args.chunks),
-    )
-    calls = (
-        lambda: m.moe_route(sh, idx, buf.expert_count, buf.send_off, buf.expert_send_off,
-                            buf.slot_row, buf.grp_off, buf.seg_off, buf.csend_off, buf.m_sizes,
-                            buf.status),
+    route = lambda: m.moe_route(sh, idx, buf.expert_count, buf.send_off,  # noqa: E731
+                                buf.expert_send_off, buf.slot_row, buf.grp_off, buf.seg_off,
+                                buf.csend_off, buf.m_sizes, buf.status)
+    fused_calls = (route, lambda: m.moe_dispatch_send_recv(sh, tens),
+                   lambda: m.moe_combine(sh, tens))
+    separate_calls = (
+        route,
         lambda: m.moe_dispatch_send(sh, x, buf.slot_row, buf.send_q, buf.send_s, buf.send_tok,
                                     buf.status),
         lambda: m.moe_dispatch_recv(sh, buf.send_q, buf.send_s, buf.send_tok, buf.expert_count,
@@ -327,44 +338,39 @@ def run_ours(args) -> None:
                                    buf.csend_off, buf.out, buf.status),
     )
 
-    def step(ev=None):
-        """The five calls one by one (an event after each when timing them)."""
+    def run_calls(calls, ev=None):
         for i, c in enumerate(calls):
             c()
             if ev is not None:
                 ev[i + 1].record(stream)
 
-    def step_pipelined():
-        """The same work as step(): moe_dispatch then moe_combine."""
-        for c in pipelined:
-            c()
+    def step_fused():
+        """The headline step through the public API: moe_dispatch + moe_combine."""
+        m.moe_dispatch(sh, tens)
+        m.moe_combine(sh, tens)
 
     K = args.steps
     W_ = max(args.warmup, 3)
 
-    # The headline step is the pipelined form (moe_dispatch, moe_combine),
-    # captured once as a CUDA graph (the library never waits on the host, so
-    # the sequence captures); replays run exactly those kernels.
-    graph = None
-    if not args.eager:
-        cap_stream = torch.cuda.Stream(device=dev)
-        cap_stream.wait_stream(stream)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=cap_stream):
-            step_pipelined()
+    # Each step form captured once as a CUDA graph (the library never waits on
+    # the host, so the sequences capture); replays run exactly those kernels.
+    def capture(fn):
+        if args.eager:
+            return fn
+        cs = torch.cuda.Stream(device=dev)
+        cs.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cs):
+            fn()
         torch.cuda.synchronize()
+        return g.replay
 
-    def run_once():
-        if graph is not None:
-            graph.replay()
-        else:
-            step_pipelined()
-
+    fused_once = capture(step_fused)
+    separate_once = capture(lambda: run_calls(separate_calls))
     for _ in range(W_):
-        flush.zero_()
-        run_once()
-        flush.zero_()
-        step()
+        for f in (fused_once, separate_once):
+            flush.zero_()
+            f()
     torch.cuda.synchronize()
 
     xh = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
@@ -379,32 +385,40 @@ def run_ours(args) -> None:
     def ev_pair():
         return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
+    def time_steps(fn, n):
+        evs = [ev_pair() for _ in range(n)]
+        for k in range(n):
+            flush.zero_()
+            evs[k][0].record(stream)
+            fn()
+            evs[k][1].record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    def time_kernels(calls, n):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+               for _ in range(n)]
+        for k in range(n):
+            flush.zero_()
+            evs[k][0].record(stream)
+            run_calls(calls, evs[k])
+        torch.cuda.synchronize()
+        return [[ev[i].elapsed_time(ev[i + 1]) for ev in evs] for i in range(len(calls))]
+
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(gpu_id(local)) as clk:
         # (1) headline: whole steps, L2 flushed before each (outside the window)
-        st_ev = [ev_pair() for _ in range(K)]
         t_wall = time.perf_counter()
-        for k in range(K):
-            flush.zero_()
-            st_ev[k][0].record(stream)
-            run_once()
-            st_ev[k][1].record(stream)
-        torch.cuda.synchronize()
+        step_ms = time_steps(fused_once, K)
         t_wall = time.perf_counter() - t_wall
         barrier(world)
-        step_ms = [a.elapsed_time(b) for a, b in st_ev]
-
-        # (2) per-kernel breakdown: eager launches, an event after each call
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(KERNELS) + 1)]
-               for _ in range(K)]
-        for k in range(K):
-            flush.zero_()
-            evs[k][0].record(stream)
-            step(evs[k])
-        torch.cuda.synchronize()
-
-        # (3) end to end through the public API with host buffers: pinned
+        # (2) the same outputs through the separate calls of the pages' steps
+        sep_ms = time_steps(separate_once, K)
+        # (3) per-kernel breakdowns: eager launches, an event after each call
+        fused_k = time_kernels(fused_calls, K)
+        sep_k = time_kernels(separate_calls, K)
+        # (4) end to end through the public API with host buffers: pinned
         # host -> device copies of the step's inputs and the device -> host
         # read of its output inside the window
         e2e_ms = []
@@ -423,28 +437,26 @@ def run_ours(args) -> None:
             if k >= W_:
                 e2e_ms.append(e0.elapsed_time(e1))
 
-    per_kernel_ms = {name: [ev[i].elapsed_time(ev[i + 1]) for ev in evs]
-                     for i, name in enumerate(KERNELS)}
-    eager_ms = statistics.mean(ev[0].elapsed_time(ev[-1]) for ev in evs)
     mean_step_ms = max_over_ranks(statistics.mean(step_ms), world)
+    sep_step_ms = max_over_ranks(statistics.mean(sep_ms), world)
     e2e_us = max_over_ranks(statistics.mean(e2e_ms), world) * 1000
     h2d = xh.numel() * xh.element_size() + ih.numel() * 4 + wh.numel() * 4
     d2h = oh.numel() * oh.element_size()
     status = int(buf.status.item())
     if status != 0:
         raise RuntimeError(f"device status {status}: {m.strerror(status)}")
-
     if rank != 0:
         return
+
     peak, peak_kind = measured_peak()
     us = mean_step_ms * 1000
-    achieved = nbytes["total"] / (us * 1e-6) / 1e9
-    avg = {n: statistics.mean(per_kernel_ms[n]) for n in KERNELS}
-    # dominant kernel: the largest share of the step
-    dom = max(("dispatch_send", "dispatch_recv", "combine_send", "combine_recv"), key=avg.get)
-    dom_gbs = nbytes["per_kernel"][dom] / (avg[dom] * 1e-3) / 1e9
-    disp_us = sum(avg[n] for n in KERNELS[:3]) * 1000
-    comb_us = sum(avg[n] for n in KERNELS[3:]) * 1000
+    moved = sum(nbytes["fused"].values())
+    s8d = nbytes["s8d_dispatch"] + nbytes["s8d_combine"]
+    achieved = moved / (us * 1e-6) / 1e9
+    favg = {n: statistics.mean(v) for n, v in zip(FUSED, fused_k)}
+    savg = {n: statistics.mean(v) for n, v in zip(KERNELS, sep_k)}
+    dom = max(("dispatch_fused", "combine_fused"), key=favg.get)
+    dom_gbs = nbytes["fused"][dom] / (favg[dom] * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": round(us, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": W_, "ms_per_step": round(mean_step_ms, 5),
@@ -456,26 +468,30 @@ def run_ours(args) -> None:
                                f"{'per-expert scale' if mode else 'identity'}",
                    "N": w.N, "T": w.T, "H": w.H, "E": w.E, "R": w.R, "cap": buf.cap,
                    "l2": "flushed before every step (512 MiB write, outside the timed window)",
+                   "path": "moe_dispatch + moe_combine (fused calls; all outputs of the six "
+                           "separate calls written every step)",
                    "parallelism": "ranks simulated as slices of one GPU; replicas across GPUs"},
-        "timing": ("CUDA-graph replay of moe_dispatch + moe_combine" if graph is not None
-                   else "eager moe_dispatch + moe_combine"),
-        "chunks": args.chunks,
-        "separate_calls_us_with_kernel_events": round(eager_ms * 1000, 2),
-        "dispatch_us": round(disp_us, 2), "combine_us": round(comb_us, 2),
+        "timing": "CUDA-graph replay" if not args.eager else "eager launches",
+        "separate_calls_us": round(sep_step_ms * 1000, 2),
+        "dispatch_us": round((favg["route"] + favg["dispatch_fused"]) * 1000, 2),
+        "combine_us": round(favg["combine_fused"] * 1000, 2),
         "achieved_gbs": round(achieved, 1),
         "frac_of_peak": round(achieved / peak, 4), "peak_gbs": peak, "peak_kind": peak_kind,
         "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
-        "algorithmic_mb": {"dispatch": round(nbytes["dispatch"] / 1e6, 1),
-                           "combine": round(nbytes["combine"] / 1e6, 1)},
-        "kernel_us": {n: round(avg[n] * 1000, 2) for n in KERNELS},
+        "bytes_moved_mb": {k: round(v / 1e6, 1) for k, v in nbytes["fused"].items()},
+        "algorithmic_mb_s8d": {"dispatch": round(nbytes["s8d_dispatch"] / 1e6, 1),
+                               "combine": round(nbytes["s8d_combine"] / 1e6, 1)},
+        "effective_gbs_s8d": round(s8d / (us * 1e-6) / 1e9, 1),
+        "kernel_us": {n: round(v * 1000, 2) for n, v in favg.items()},
+        "separate_kernel_us": {n: round(v * 1000, 2) for n, v in savg.items()},
         "roofline": {"bound": "hbm", "kernel": KERNEL_SYMBOL[dom],
                      "achieved": round(dom_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(dom_gbs / peak, 4),
                      "traffic": dram_traffic(dom, args.config),
-                     "algorithmic_bytes": nbytes["per_kernel"][dom]},
+                     "algorithmic_bytes": nbytes["fused"][dom]},
         "e2e": {"value": round(e2e_us, 2), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": len(KERNELS) * K,  # our kernels in the headline timed region
+        "gpu_launches": len(FUSED) * K,  # our kernels in the headline timed region
         "clocks": clk.summary(),
         "status": status,
         "wall_s_timed": round(t_wall, 3),
@@ -495,8 +511,6 @@ def main() -> None:
     ap.add_argument("--config", default="dsv3_decode")
     ap.add_argument("--cap", type=int, default=0,
                     help="grouped rows per rank (0: N*T*min(R,E/N), the library default)")
-    ap.add_argument("--chunks", type=int, default=0,
-                    help="sender chunks of the pipelined calls (0: sized to L2, 1: none)")
     ap.add_argument("--eager", action="store_true",
                     help="time eager launches instead of CUDA-graph replays")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")

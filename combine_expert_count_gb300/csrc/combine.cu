@@ -100,14 +100,103 @@ __global__ void __launch_bounds__(kReduceThreads)
 cudaError_t launch_combine_reduce(const moe_shape &sh, int cap, const uint16_t *csend,
                                   const int32_t *idx, const float *w, const int32_t *slot_row,
                                   const int32_t *send_off, const int32_t *csend_off,
-                                  uint16_t *out, cudaStream_t st, long long tok0, long long tok1) {
-    if (tok1 < 0) tok1 = (long long)sh.N * sh.T;
-    const long long ntok = tok1 - tok0;
+                                  uint16_t *out, cudaStream_t st) {
+    const long long ntok = (long long)sh.N * sh.T;
     if (ntok <= 0) return cudaSuccess;
     const int grid = (int)(ntok < (1LL << 30) ? ntok : (1LL << 30));
     return launch_kernel(k_combine_reduce, dim3((unsigned)grid), dim3(kReduceThreads), 0, st,
-                         sh.N, sh.T, sh.E, sh.R, sh.H, cap, tok0, tok1, csend, idx, w, slot_row,
+                         sh.N, sh.T, sh.E, sh.R, sh.H, cap, 0LL, ntok, csend, idx, w, slot_row,
                          send_off, csend_off, out);
+}
+
+// ------------------------------------------------------------ fused combine
+//
+// combine_send and combine_recv in one pass.  For token t of rank s and slot
+// k (expert e on rank p), the expert output sits at grouped row
+// g = seg_off[p][j][s] + (slot - expert_send_off[s][e]) of y and belongs at
+// combine row c = csend_off[p][s] + (slot - send_off[s][p]).  The block
+// reads each of the token's R rows once from y, writes it to its csend row
+// (so the combine send buffer is produced exactly as by moe_combine_send) and
+// folds the same values into the fp32 accumulator in slot order, as
+// moe_combine_recv would after reading them back.  A row whose grouped
+// position was dropped is written as zeros and contributes w * 0.
+__global__ void __launch_bounds__(kReduceThreads)
+    k_combine_fused(int N, int T, int E, int R, int H, int cap, const uint16_t *__restrict__ y,
+                    const int32_t *__restrict__ idx, const float *__restrict__ w,
+                    const int32_t *__restrict__ slot_row, const int32_t *__restrict__ eso,
+                    const int32_t *__restrict__ seg_off, const int32_t *__restrict__ send_off,
+                    const int32_t *__restrict__ csend_off, uint16_t *__restrict__ csend,
+                    uint16_t *__restrict__ out) {
+    __shared__ long long ysrc[MOE_MAX_TOPK];  // element offset of the row in y, -1: zeros
+    __shared__ long long cdst[MOE_MAX_TOPK];  // element offset in csend, -1: not sent
+    __shared__ float wk[MOE_MAX_TOPK];
+    const int Er = E / N, cpr = H >> 3;
+    const long long ntok = (long long)N * T;
+    for (long long tok = blockIdx.x; tok < ntok; tok += gridDim.x) {
+        const int s = (int)div_nonneg(tok, T);
+        if (threadIdx.x < R) {
+            const int k = threadIdx.x;
+            const int e = __ldg(idx + tok * R + k);
+            const int sl = __ldg(slot_row + tok * R + k);
+            long long yo = -1, co = -1;
+            if ((unsigned)e < (unsigned)E && sl >= 0) {
+                const int p = e / Er, j = e - p * Er;
+                const int c = __ldg(csend_off + (size_t)p * (N + 1) + s) +
+                              (sl - __ldg(send_off + (size_t)s * (N + 1) + p));
+                if (c >= 0 && c < cap) {
+                    co = ((long long)p * cap + c) * H;
+                    const int g = __ldg(seg_off + ((size_t)p * Er + j) * N + s) +
+                                  (sl - __ldg(eso + (size_t)s * (E + 1) + e));
+                    if (g >= 0 && g < cap) yo = ((long long)p * cap + g) * H;
+                }
+            }
+            ysrc[k] = yo;
+            cdst[k] = co;
+            wk[k] = __ldg(w + tok * R + k);
+        }
+        __syncthreads();
+        for (int part = threadIdx.x; part < cpr; part += blockDim.x) {
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int k0 = 0; k0 < R; k0 += kReduceGroup) {
+                uint4 v[kReduceGroup];
+#pragma unroll
+                for (int u = 0; u < kReduceGroup; ++u) {
+                    const int k = k0 + u;
+                    v[u] = make_uint4(0, 0, 0, 0);
+                    if (k < R && ysrc[k] >= 0)
+                        v[u] = __ldcs(reinterpret_cast<const uint4 *>(y + ysrc[k]) + part);
+                }
+#pragma unroll
+                for (int u = 0; u < kReduceGroup; ++u) {
+                    const int k = k0 + u;
+                    if (k < R && cdst[k] >= 0) {
+                        reinterpret_cast<uint4 *>(csend + cdst[k])[part] = v[u];
+                        fma8(acc, wk[k], v[u]);
+                    }
+                }
+            }
+            uint4 o;
+            o.x = pack_bf16x2(acc[0], acc[1]);
+            o.y = pack_bf16x2(acc[2], acc[3]);
+            o.z = pack_bf16x2(acc[4], acc[5]);
+            o.w = pack_bf16x2(acc[6], acc[7]);
+            reinterpret_cast<uint4 *>(out + tok * H)[part] = o;
+        }
+        __syncthreads();
+    }
+}
+
+cudaError_t launch_combine_fused(const moe_shape &sh, int cap, const uint16_t *y,
+                                 const int32_t *idx, const float *w, const int32_t *slot_row,
+                                 const int32_t *eso, const int32_t *seg_off,
+                                 const int32_t *send_off, const int32_t *csend_off,
+                                 uint16_t *csend, uint16_t *out, cudaStream_t st) {
+    const long long ntok = (long long)sh.N * sh.T;
+    if (ntok <= 0) return cudaSuccess;
+    const int grid = (int)(ntok < (1LL << 30) ? ntok : (1LL << 30));
+    return launch_kernel(k_combine_fused, dim3((unsigned)grid), dim3(kReduceThreads), 0, st, sh.N,
+                         sh.T, sh.E, sh.R, sh.H, cap, y, idx, w, slot_row, eso, seg_off, send_off,
+                         csend_off, csend, out);
 }
 
 // ------------------------------------------------------------ expert stand-in

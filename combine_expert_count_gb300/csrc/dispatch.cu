@@ -53,11 +53,45 @@ __device__ __forceinline__ float amax16(const uint4 &a, const uint4 &b) {
     return m;
 }
 
+// Where the grouped copy of each assignment goes, for the fused dispatch:
+// row i = slot of rank s for expert e lands at grouped row
+// seg_off[r][j][s] + (i - expert_send_off[s][e]) of rank r = e / Er.
+struct GroupedDest {
+    int N, E, cap;
+    const int32_t *idx, *eso, *seg_off;
+    uint8_t *grp_q;
+    float *grp_s;
+    int32_t *grp_src;
+};
+
+// Send row and grouped row of assignment k of token tok (-1: none).
+template <bool kGrouped>
+__device__ __forceinline__ void dest_rows(long long tok, int k, int T, int R, long long TR,
+                                          const int32_t *__restrict__ slot_row,
+                                          const GroupedDest &gd, long long &row,
+                                          long long &grow) {
+    const long long s = div_nonneg(tok, T);
+    const int sr = __ldg(slot_row + tok * R + k);
+    row = (sr >= 0 && sr < TR) ? s * TR + sr : -1;
+    grow = -1;
+    if (kGrouped && row >= 0) {
+        const int e = __ldg(gd.idx + tok * R + k);
+        if ((unsigned)e < (unsigned)gd.E) {
+            const int Er = gd.E / gd.N, r = e / Er, j = e - r * Er;
+            const int g = __ldg(gd.seg_off + ((size_t)r * Er + j) * gd.N + s) +
+                          (sr - __ldg(gd.eso + (size_t)s * (gd.E + 1) + e));
+            if (g >= 0 && g < gd.cap) grow = (long long)r * gd.cap + g;
+        }
+    }
+}
+
+template <bool kGrouped>
 __global__ void __launch_bounds__(256)
     k_quant_pack_staged(int T, int R, int H, int P, long long tok0, long long nitems,
                         const uint16_t *__restrict__ x, const int32_t *__restrict__ slot_row,
                         uint8_t *__restrict__ send_q, float *__restrict__ send_s,
-                        int32_t *__restrict__ send_tok, int32_t *__restrict__ status) {
+                        int32_t *__restrict__ send_tok, int32_t *__restrict__ status,
+                        const GroupedDest gd) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     unsigned char *sm = align128(smem_raw);
     uint16_t *xbuf = reinterpret_cast<uint16_t *>(sm);            // [2][P] bf16
@@ -65,6 +99,7 @@ __global__ void __launch_bounds__(256)
     float *sbuf = reinterpret_cast<float *>(sm + (size_t)6 * P);  // [2][P/128]
     __shared__ uint64_t xbar[2];
     __shared__ long long rows[2][MOE_MAX_TOPK];
+    __shared__ long long grows[2][MOE_MAX_TOPK];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthr = blockDim.x;
     const int Sb = H >> 7, npieces = (H + P - 1) / P;
@@ -89,10 +124,11 @@ __global__ void __launch_bounds__(256)
     const long long first = blockIdx.x, G = gridDim.x;
     if (tid == 0 && first < nitems) issue_load(first, 0);
     bool timed_out = false;
-    // thread tid < R: the slot of the current item, read one item ahead
-    int pref = -1;
+    // thread tid < R: destinations of the current item, read one item ahead
+    long long prow = -1, pgrow = -1;
     if (tid < R && first < nitems)
-        pref = __ldg(slot_row + (tok0 + div_nonneg(first, npieces)) * R + tid);
+        dest_rows<kGrouped>(tok0 + div_nonneg(first, npieces), tid, T, R, TR, slot_row, gd, prow,
+                            pgrow);
 
     int n = 0;
     for (long long item = first; item < nitems; item += G, ++n) {
@@ -134,10 +170,14 @@ __global__ void __launch_bounds__(256)
             }
         }
         fence_proxy_async_smem();
-        if (tid < R) rows[b][tid] = (pref >= 0 && pref < TR) ? s * TR + pref : -1;
+        if (tid < R) {
+            rows[b][tid] = prow;
+            grows[b][tid] = pgrow;
+        }
         __syncthreads();
         if (tid < R && item + G < nitems)
-            pref = __ldg(slot_row + (tok0 + div_nonneg(item + G, npieces)) * R + tid);
+            dest_rows<kGrouped>(tok0 + div_nonneg(item + G, npieces), tid, T, R, TR, slot_row, gd,
+                                prow, pgrow);
         if (tid == 0) {
             for (int k = 0; k < R; ++k) {
                 const long long row = rows[b][k];
@@ -145,17 +185,31 @@ __global__ void __launch_bounds__(256)
                 bulk_s2g(send_q + row * H + off, qs, (uint32_t)len);
                 if (bulk_scales)
                     bulk_s2g(send_s + row * Sb + (off >> 7), ss, (uint32_t)(len >> 7) * 4u);
+                if (kGrouped) {
+                    const long long grow = grows[b][k];
+                    if (grow < 0) continue;
+                    bulk_s2g(gd.grp_q + grow * H + off, qs, (uint32_t)len);
+                    if (bulk_scales)
+                        bulk_s2g(gd.grp_s + grow * Sb + (off >> 7), ss, (uint32_t)(len >> 7) * 4u);
+                }
             }
             bulk_commit();
         }
         if (!bulk_scales) {
             const int nb = len >> 7;
             for (int i = tid; i < R * nb; i += nthr) {
-                const long long row = rows[b][i / nb];
-                if (row >= 0) send_s[row * Sb + (off >> 7) + i % nb] = ss[i % nb];
+                const int k = i / nb, blk = i - k * nb;
+                const long long row = rows[b][k];
+                if (row >= 0) send_s[row * Sb + (off >> 7) + blk] = ss[blk];
+                if (kGrouped && grows[b][k] >= 0)
+                    gd.grp_s[grows[b][k] * Sb + (off >> 7) + blk] = ss[blk];
             }
         }
-        if (piece == 0 && tid < R && rows[b][tid] >= 0) send_tok[rows[b][tid]] = t;
+        if (piece == 0 && tid < R && rows[b][tid] >= 0) {
+            send_tok[rows[b][tid]] = t;
+            if (kGrouped && grows[b][tid] >= 0)
+                *reinterpret_cast<int2 *>(gd.grp_src + grows[b][tid] * 2) = make_int2((int)s, t);
+        }
     }
     if (tid == 0) {
         bulk_wait_all();
@@ -176,12 +230,13 @@ static int quant_threads(int nch) {
     return nch >= 256 ? 256 : 32 * ((nch + 31) / 32);
 }
 
-cudaError_t launch_quant_pack(const moe_shape &sh, const uint16_t *x, const int32_t *slot_row,
-                              uint8_t *send_q, float *send_s, int32_t *send_tok, int32_t *status,
-                              cudaStream_t st, long long tok0, long long tok1) {
-    if (tok1 < 0) tok1 = (long long)sh.N * sh.T;
-    const long long ntok = tok1 - tok0;
+template <bool kGrouped>
+static cudaError_t launch_staged(const moe_shape &sh, const uint16_t *x, const int32_t *slot_row,
+                                 uint8_t *send_q, float *send_s, int32_t *send_tok,
+                                 int32_t *status, const GroupedDest &gd, cudaStream_t st) {
+    const long long ntok = (long long)sh.N * sh.T;
     if (ntok <= 0) return cudaSuccess;
+    auto kern = k_quant_pack_staged<kGrouped>;
     const int P = sh.H < kPieceElems ? sh.H : kPieceElems;
     const long long nitems = ntok * ((sh.H + P - 1) / P);
     const int threads = quant_threads(P / 16);
@@ -191,11 +246,10 @@ cudaError_t launch_quant_pack(const moe_shape &sh, const uint16_t *x, const int3
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev != cached_dev || smem != cached_smem || threads != cached_threads) {
-        err = cudaFuncSetAttribute(k_quant_pack_staged, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   smem);
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (err != cudaSuccess) return err;
         int occ = 0;
-        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_quant_pack_staged, threads, smem);
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
         if (err != cudaSuccess) return err;
         cached_occ = occ < 1 ? 1 : occ;
         cached_dev = dev;
@@ -204,9 +258,33 @@ cudaError_t launch_quant_pack(const moe_shape &sh, const uint16_t *x, const int3
     }
     long long grid = (long long)sm_count() * cached_occ;
     if (grid > nitems) grid = nitems;
-    return launch_kernel(k_quant_pack_staged, dim3((unsigned)grid), dim3(threads), (size_t)smem,
-                         st, sh.T, sh.R, sh.H, P, tok0, nitems, x, slot_row, send_q, send_s,
-                         send_tok, status);
+    return launch_kernel(kern, dim3((unsigned)grid), dim3(threads), (size_t)smem, st, sh.T, sh.R,
+                         sh.H, P, 0LL, nitems, x, slot_row, send_q, send_s, send_tok, status, gd);
+}
+
+cudaError_t launch_quant_pack(const moe_shape &sh, const uint16_t *x, const int32_t *slot_row,
+                              uint8_t *send_q, float *send_s, int32_t *send_tok, int32_t *status,
+                              cudaStream_t st) {
+    GroupedDest gd = {};
+    return launch_staged<false>(sh, x, slot_row, send_q, send_s, send_tok, status, gd, st);
+}
+
+cudaError_t launch_dispatch_fused(const moe_shape &sh, int cap, const uint16_t *x,
+                                  const int32_t *idx, const int32_t *slot_row, const int32_t *eso,
+                                  const int32_t *seg_off, uint8_t *send_q, float *send_s,
+                                  int32_t *send_tok, uint8_t *grp_q, float *grp_s,
+                                  int32_t *grp_src, int32_t *status, cudaStream_t st) {
+    GroupedDest gd;
+    gd.N = sh.N;
+    gd.E = sh.E;
+    gd.cap = cap;
+    gd.idx = idx;
+    gd.eso = eso;
+    gd.seg_off = seg_off;
+    gd.grp_q = grp_q;
+    gd.grp_s = grp_s;
+    gd.grp_src = grp_src;
+    return launch_staged<true>(sh, x, slot_row, send_q, send_s, send_tok, status, gd, st);
 }
 
 }  // namespace moe

@@ -25,7 +25,15 @@ cudaError_t launch_exchange(const moe_shape &sh, int cap, const int32_t *cnt,
 
 cudaError_t launch_quant_pack(const moe_shape &sh, const uint16_t *x, const int32_t *slot_row,
                               uint8_t *send_q, float *send_s, int32_t *send_tok, int32_t *status,
-                              cudaStream_t st, long long tok0 = 0, long long tok1 = -1);
+                              cudaStream_t st);
+
+// Quantise + pack + receive shuffle in one pass: the fp8 rows go to the send
+// buffer and, at the same time, to their grouped rows (moe_dispatch).
+cudaError_t launch_dispatch_fused(const moe_shape &sh, int cap, const uint16_t *x,
+                                  const int32_t *idx, const int32_t *slot_row, const int32_t *eso,
+                                  const int32_t *seg_off, uint8_t *send_q, float *send_s,
+                                  int32_t *send_tok, uint8_t *grp_q, float *grp_s,
+                                  int32_t *grp_src, int32_t *status, cudaStream_t st);
 
 cudaError_t launch_dispatch_pull(const moe_shape &sh, int cap, const uint8_t *send_q,
                                  const float *send_s, const int32_t *send_tok,
@@ -42,8 +50,14 @@ cudaError_t launch_combine_pack(const moe_shape &sh, int cap, const uint16_t *y,
 cudaError_t launch_combine_reduce(const moe_shape &sh, int cap, const uint16_t *csend,
                                   const int32_t *idx, const float *w, const int32_t *slot_row,
                                   const int32_t *send_off, const int32_t *csend_off,
-                                  uint16_t *out, cudaStream_t st, long long tok0 = 0,
-                                  long long tok1 = -1);
+                                  uint16_t *out, cudaStream_t st);
+
+// Combine send + receive in one pass (moe_combine).
+cudaError_t launch_combine_fused(const moe_shape &sh, int cap, const uint16_t *y,
+                                 const int32_t *idx, const float *w, const int32_t *slot_row,
+                                 const int32_t *eso, const int32_t *seg_off,
+                                 const int32_t *send_off, const int32_t *csend_off,
+                                 uint16_t *csend, uint16_t *out, cudaStream_t st);
 
 cudaError_t launch_expert_standin(const moe_shape &sh, int cap, int mode, const uint8_t *grp_q,
                                   const float *grp_s, const int32_t *grp_off, uint16_t *y,

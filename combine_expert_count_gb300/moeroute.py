@@ -10,9 +10,9 @@ CUDA kernels; there is no other implementation to fall back on, and importing
 a function without the built library raises.
 
 ``MoeBuffers`` owns one set of device buffers for a shape (PyTorch is the
-allocator) and strings the calls together in the pages' order for callers who
-want the whole path:  ``dispatch`` = route_count, exchange, dispatch_send,
-dispatch_recv;  ``combine`` = combine_send, combine_recv.
+allocator) and strings the calls together for callers who want the whole
+path:  ``dispatch`` = moe_dispatch (or route_count, exchange, dispatch_send,
+dispatch_recv);  ``combine`` = moe_combine (or combine_send, combine_recv).
 """
 from __future__ import annotations
 
@@ -31,7 +31,7 @@ MOE_ST_BAD_EXPERT, MOE_ST_CAPACITY, MOE_ST_TIMEOUT = 1, 2, 4
 
 EXPORTS = ("moe_sizes_query", "moe_route_count", "moe_exchange", "moe_route", "moe_dispatch_send",
            "moe_dispatch_recv", "moe_combine_send", "moe_combine_recv", "moe_dispatch",
-           "moe_combine", "moe_expert_standin", "moe_e4m3_encode", "moe_strerror", "moe_version")
+           "moe_dispatch_send_recv", "moe_combine", "moe_expert_standin", "moe_e4m3_encode", "moe_strerror", "moe_version")
 
 
 class moe_shape(ctypes.Structure):
@@ -83,8 +83,9 @@ def lib() -> ctypes.CDLL:
             h.moe_route_count.argtypes = [sp] + [V] * 6 + [V]
             h.moe_exchange.argtypes = [sp] + [V] * 7 + [V]
             h.moe_route.argtypes = [sp] + [V] * 10 + [V]
-            h.moe_dispatch.argtypes = [sp, P(moe_buffers), I, V]
-            h.moe_combine.argtypes = [sp, P(moe_buffers), I, V]
+            h.moe_dispatch.argtypes = [sp, P(moe_buffers), V]
+            h.moe_dispatch_send_recv.argtypes = [sp, P(moe_buffers), V]
+            h.moe_combine.argtypes = [sp, P(moe_buffers), V]
             h.moe_dispatch_send.argtypes = [sp] + [V] * 6 + [V]
             h.moe_dispatch_recv.argtypes = [sp] + [V] * 10 + [V]
             h.moe_combine_send.argtypes = [sp] + [V] * 8 + [V]
@@ -264,22 +265,28 @@ def _buffers(z: moe_sizes, tensors: dict, needs: dict) -> moe_buffers:
     return b
 
 
-def moe_dispatch(shape, tensors: dict, chunks: int = 0, stream=None) -> None:
+def moe_dispatch(shape, tensors: dict, stream=None) -> None:
     """Whole dispatch in one call; ``tensors`` maps moe_buffers field names
     (x, topk_idx, routing arrays, send and grouped buffers, status) to tensors."""
     sh, z = _as_shape(shape), sizes_query(shape)
     b = _buffers(z, tensors, _DISPATCH_NEEDS)
-    _check(lib().moe_dispatch(ctypes.byref(sh), ctypes.byref(b), int(chunks), _s(stream)),
-           "moe_dispatch")
+    _check(lib().moe_dispatch(ctypes.byref(sh), ctypes.byref(b), _s(stream)), "moe_dispatch")
 
 
-def moe_combine(shape, tensors: dict, chunks: int = 0, stream=None) -> None:
+def moe_dispatch_send_recv(shape, tensors: dict, stream=None) -> None:
+    """Quantise + pack + receive shuffle in one kernel (routing arrays given)."""
+    sh, z = _as_shape(shape), sizes_query(shape)
+    b = _buffers(z, tensors, _DISPATCH_NEEDS)
+    _check(lib().moe_dispatch_send_recv(ctypes.byref(sh), ctypes.byref(b), _s(stream)),
+           "moe_dispatch_send_recv")
+
+
+def moe_combine(shape, tensors: dict, stream=None) -> None:
     """Whole combine in one call; ``tensors`` as for moe_dispatch (y, topk_idx,
     topk_w, routing arrays, csend, out, status)."""
     sh, z = _as_shape(shape), sizes_query(shape)
     b = _buffers(z, tensors, _COMBINE_NEEDS)
-    _check(lib().moe_combine(ctypes.byref(sh), ctypes.byref(b), int(chunks), _s(stream)),
-           "moe_combine")
+    _check(lib().moe_combine(ctypes.byref(sh), ctypes.byref(b), _s(stream)), "moe_combine")
 
 
 def moe_expert_standin(shape, mode: int, grp_q, grp_s, grp_off, y, stream=None) -> None:
@@ -358,13 +365,12 @@ class MoeBuffers:
         d.update(extra)
         return d
 
-    def dispatch(self, x, topk_idx, stream=None, calls: str = "pipelined",
-                 chunks: int = 0) -> None:
-        """The dispatch half.  ``calls``: "pipelined" (one moe_dispatch call,
-        sender chunks through L2), "fused_route" (moe_route then the two
-        dispatch calls) or "separate" (the four calls of the pages' steps)."""
-        if calls == "pipelined":
-            moe_dispatch(self.shape, self.tensors(x=x, topk_idx=topk_idx), chunks, stream)
+    def dispatch(self, x, topk_idx, stream=None, calls: str = "fused") -> None:
+        """The dispatch half.  ``calls``: "fused" (one moe_dispatch call),
+        "fused_route" (moe_route then the two dispatch calls) or "separate"
+        (the four calls of the pages' steps)."""
+        if calls == "fused":
+            moe_dispatch(self.shape, self.tensors(x=x, topk_idx=topk_idx), stream)
             return
         self.route(topk_idx, stream, calls == "fused_route")
         moe_dispatch_send(self.shape, x, self.slot_row, self.send_q, self.send_s, self.send_tok,
@@ -377,16 +383,15 @@ class MoeBuffers:
         """The grouped-GEMM stand-in (identity or per-expert scale)."""
         moe_expert_standin(self.shape, mode, self.grp_q, self.grp_s, self.grp_off, self.y, stream)
 
-    def combine(self, topk_idx, topk_w, y=None, out=None, stream=None, calls: str = "pipelined",
-                chunks: int = 0) -> torch.Tensor:
-        """The combine half; returns ``out``.  ``calls``: "pipelined" (one
+    def combine(self, topk_idx, topk_w, y=None, out=None, stream=None,
+                calls: str = "fused") -> torch.Tensor:
+        """The combine half; returns ``out``.  ``calls``: "fused" (one
         moe_combine call) or anything else for moe_combine_send then
         moe_combine_recv."""
         out = self.out if out is None else out
-        if calls == "pipelined":
+        if calls == "fused":
             moe_combine(self.shape, self.tensors(topk_idx=topk_idx, topk_w=topk_w,
-                                                 y=self.y if y is None else y, out=out),
-                        chunks, stream)
+                                                 y=self.y if y is None else y, out=out), stream)
             return out
         moe_combine_send(self.shape, self.y if y is None else y, self.expert_count,
                          self.expert_send_off, self.send_off, self.seg_off, self.csend_off,

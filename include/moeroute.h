@@ -230,12 +230,18 @@ int moe_expert_standin(const moe_shape *shape, int mode, const uint8_t *grp_q,
  * be compared with other implementations. */
 int moe_e4m3_encode(const float *v, uint8_t *out, int64_t n, void *stream);
 
-/* ---------------------------------------------------------------- pipelined
- * The whole dispatch and the whole combine as one call each.  Outputs are
- * exactly those of the separate calls above (route + dispatch_send +
- * dispatch_recv; combine_send + combine_recv).  Optionally the senders are
- * taken in chunks of consecutive ranks, each chunk's producer followed by its
- * consumer so the consumer reads rows the producer just left in L2. */
+/* ---------------------------------------------------------------- fused
+ * The whole dispatch and the whole combine as one call each, with the same
+ * outputs, bit for bit, as the separate calls above.  They differ in how the
+ * bytes move: moe_dispatch quantises each token once and writes its fp8 rows
+ * to the send buffer and to their grouped rows in the same pass (the receive
+ * shuffle never re-reads the send buffer); moe_combine reads each expert
+ * output row once, writes it to its combine send row and accumulates it into
+ * the token's output in the same pass (the combine send buffer is written but
+ * not read back).  On the pages each sender learns the receivers' offsets
+ * from the routing exchange and writes its tokens straight to their places
+ * ("Send and receive buffers"); with every rank in one GPU's memory that
+ * knowledge lets the quantiser place each row at its final position. */
 typedef struct {
     const int32_t *topk_idx;   /* [N][T][R] */
     const float *topk_w;       /* [N][T][R] (combine) */
@@ -260,18 +266,22 @@ typedef struct {
     int32_t *status;           /* one int32 */
 } moe_buffers;
 
-/* moe_route, then for each chunk of senders: moe_dispatch_send of the
- * chunk's tokens, moe_dispatch_recv of the chunk's send rows.  Uses x,
- * topk_idx, the routing arrays, the send buffers and the grouped buffers.
- * chunks = 0 or 1: no chunking; chunks > 1 splits the N ranks into that many
- * near-equal chunks. */
-int moe_dispatch(const moe_shape *shape, const moe_buffers *b, int chunks, void *stream);
+/* moe_dispatch_send and moe_dispatch_recv in one kernel, given the routing
+ * arrays of a moe_route (or moe_route_count + moe_exchange) of the same
+ * topk_idx: each token is quantised once and its fp8 rows, scales and ids go
+ * to the send buffer and to their grouped rows.  Does not clear *status. */
+int moe_dispatch_send_recv(const moe_shape *shape, const moe_buffers *b, void *stream);
 
-/* For each chunk of destination ranks: moe_combine_send of the rows going
- * back to them, then moe_combine_recv of their tokens.  Uses y, topk_idx,
- * topk_w, the routing arrays, csend and out; the routing arrays must come
- * from a dispatch of the same topk_idx.  chunks as for moe_dispatch. */
-int moe_combine(const moe_shape *shape, const moe_buffers *b, int chunks, void *stream);
+/* moe_route, then moe_dispatch_send_recv.  Uses x,
+ * topk_idx, the routing arrays, the send buffers and the grouped buffers;
+ * *status is cleared first.  Outputs: everything moe_route_count,
+ * moe_exchange, moe_dispatch_send and moe_dispatch_recv write. */
+int moe_dispatch(const moe_shape *shape, const moe_buffers *b, void *stream);
+
+/* moe_combine_send + moe_combine_recv in one kernel.  Uses y, topk_idx,
+ * topk_w, the routing arrays (from a dispatch of the same topk_idx), csend
+ * and out.  Outputs: csend and out, as the two separate calls write them. */
+int moe_combine(const moe_shape *shape, const moe_buffers *b, void *stream);
 
 /* Static description of an error code or status bit set. */
 const char *moe_strerror(int code);

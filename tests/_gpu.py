@@ -37,16 +37,15 @@ def fill_sentinels(buf: m.MoeBuffers) -> None:
 
 
 def run_path(w: W.Workload, dd: dict, cap: int = 0, mode: int | None = None,
-             sentinels: bool = True, calls: str = "pipelined",
-             chunks: int = 0) -> m.MoeBuffers:
+             sentinels: bool = True, calls: str = "fused") -> m.MoeBuffers:
     """Whole path on the GPU: dispatch, stand-in expert, combine.  ``calls``
     picks the call form (see MoeBuffers.dispatch)."""
     buf = m.MoeBuffers(w.N, w.T, w.E, w.R, w.H, cap=cap, device="cuda")
     if sentinels:
         fill_sentinels(buf)
-    buf.dispatch(dd["x"], dd["topk_idx"], calls=calls, chunks=chunks)
+    buf.dispatch(dd["x"], dd["topk_idx"], calls=calls)
     buf.expert(mode if mode is not None else (1 if w.expert == "scale" else 0))
-    buf.combine(dd["topk_idx"], dd["topk_w"], calls=calls, chunks=chunks)
+    buf.combine(dd["topk_idx"], dd["topk_w"], calls=calls)
     torch.cuda.synchronize()
     return buf
 

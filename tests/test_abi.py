@@ -108,15 +108,13 @@ def test_null_and_misaligned_pointers_rejected(lib):
                 args = [good] * nptr
                 args[i] = p
                 assert fn(ctypes.byref(sh), *args, None) == m.MOE_EINVAL, (name, i, p)
-    for fn in (L.moe_dispatch, L.moe_combine):
-        assert fn(ctypes.byref(sh), None, 0, None) == m.MOE_EINVAL
-        needs = m._DISPATCH_NEEDS if fn is L.moe_dispatch else m._COMBINE_NEEDS
+    for fn in (L.moe_dispatch, L.moe_dispatch_send_recv, L.moe_combine):
+        assert fn(ctypes.byref(sh), None, None) == m.MOE_EINVAL
+        needs = m._COMBINE_NEEDS if fn is L.moe_combine else m._DISPATCH_NEEDS
         for field in list(needs) + ["status"]:
             b = m.moe_buffers(*([0x10000] * len(m._BUFFER_FIELDS)))
             setattr(b, field, 0x10004)
-            assert fn(ctypes.byref(sh), ctypes.byref(b), 0, None) == m.MOE_EINVAL, field
-        b = m.moe_buffers(*([0x10000] * len(m._BUFFER_FIELDS)))
-        assert fn(ctypes.byref(sh), ctypes.byref(b), -1, None) == m.MOE_EINVAL
+            assert fn(ctypes.byref(sh), ctypes.byref(b), None) == m.MOE_EINVAL, field
     assert L.moe_expert_standin(ctypes.byref(sh), 2, good, good, good, good, None) == m.MOE_EINVAL
     assert L.moe_expert_standin(ctypes.byref(sh), 0, bad, good, good, good, None) == m.MOE_EINVAL
     assert L.moe_e4m3_encode(null, good, 4, None) == m.MOE_EINVAL

@@ -22,11 +22,15 @@ from combine_expert_count_gb300 import workloads as W  # noqa: E402
 def test_algorithmic_bytes_match_formulas():
     w = W.CONFIGS["dsv3_decode"]
     b = bench.algorithmic_bytes(w, w.A)
-    assert round(b["dispatch"] / 1e6, 1) == 392.8
-    assert round(b["combine"] / 1e6, 1) == 734.1
-    per = b["per_kernel"]
+    assert round(b["s8d_dispatch"] / 1e6, 1) == 392.8
+    assert round(b["s8d_combine"] / 1e6, 1) == 734.1
+    per = b["separate"]
     assert per["combine_send"] == 4 * w.A * w.H
     assert per["dispatch_send"] > 2 * w.N * w.T * w.H
+    # the fused calls skip exactly the two re-reads
+    sep, fus = sum(b["separate"].values()), sum(b["fused"].values())
+    row8 = w.H + 4 * (w.H // 128)
+    assert abs((sep - fus) - (w.A * (row8 + 4) + w.A * 2 * w.H)) <= 24 * w.A
 
 
 def test_reference_arm_prints_one_json_line():

@@ -60,20 +60,23 @@ def test_config_full_parity(name):
 def test_other_call_forms(name, calls):
     """The per-step calls (moe_route_count, moe_exchange, moe_dispatch_send,
     moe_dispatch_recv, moe_combine_send, moe_combine_recv), and the same with
-    moe_route, give the oracle's outputs like the pipelined calls."""
+    moe_route, give the oracle's outputs like the fused calls."""
     w = W.CONFIGS[name]
     d = W.generate(w)
     buf = G.run_path(w, G.to_dev(d), calls=calls)
     G.compare_with_oracle(w, buf, _oracle(w, d, _exact_cap(w, d)))
 
 
-@pytest.mark.parametrize("chunks", [1, 2, 3, 5, 16])
-def test_pipeline_chunk_counts(chunks):
-    """Every chunking of the sender ranks gives the same outputs."""
-    w = W.CONFIGS["dsv3_decode"].replace(T=32)
+@pytest.mark.parametrize("H", [128, 640, 8192 + 1024, 20480])
+def test_fused_and_separate_identical_across_row_pieces(H):
+    """Rows longer than one shared-memory piece (8192 elements), and scale
+    rows that are not whole 16-byte vectors (H/128 not a multiple of 4), give
+    the oracle's outputs in both call forms."""
+    w = W.Workload("pieces", N=2, T=3, H=H, E=4, R=2, seed=H)
     d = W.generate(w)
-    buf = G.run_path(w, G.to_dev(d), chunks=chunks)
-    G.compare_with_oracle(w, buf, _oracle(w, d, _exact_cap(w, d)))
+    o = _oracle(w, d, w.default_cap)
+    for calls in ("fused", "separate"):
+        G.compare_with_oracle(w, G.run_path(w, G.to_dev(d), calls=calls), o)
 
 
 def test_worst_case_reduced_t_full_parity():
@@ -147,11 +150,9 @@ def test_small_shape_grid(N, T, E, R, H):
     w = W.Workload("grid", N=N, T=T, H=H, E=E, R=R, seed=7 + N * 1000 + T * 100 + E * 10 + R)
     d = W.generate(w)
     o = _oracle(w, d, w.default_cap)
-    for calls in ("pipelined", "separate", "fused_route"):
-        buf = G.run_path(w, G.to_dev(d), calls=calls, chunks=0 if calls == "pipelined" else 1)
+    for calls in ("fused", "separate", "fused_route"):
+        buf = G.run_path(w, G.to_dev(d), calls=calls)
         G.compare_with_oracle(w, buf, o)
-    buf = G.run_path(w, G.to_dev(d), chunks=N)
-    G.compare_with_oracle(w, buf, o)
 
 
 def test_empty_batch():
@@ -174,7 +175,7 @@ def test_empty_batch():
     assert np.all(G.host(buf.grp_off) == 0) and np.all(G.host(buf.csend_off) == 0)
 
 
-@pytest.mark.parametrize("calls", ["pipelined", "separate", "fused_route"])
+@pytest.mark.parametrize("calls", ["fused", "separate", "fused_route"])
 def test_bad_expert_ids_are_skipped_and_flagged(calls):
     w = W.Workload("bad", N=2, T=8, H=256, E=8, R=2, seed=3)
     d = W.generate(w)
@@ -189,11 +190,11 @@ def test_bad_expert_ids_are_skipped_and_flagged(calls):
 
 
 @pytest.mark.parametrize("cap", [1, 7, 20])
-@pytest.mark.parametrize("calls", ["pipelined", "separate", "fused_route"])
+@pytest.mark.parametrize("calls", ["fused", "separate", "fused_route"])
 def test_capacity_overflow_drops_and_flags(cap, calls):
     w = W.Workload("cap", N=2, T=16, H=256, E=4, R=2, seed=11)
     d = W.generate(w)
-    buf = G.run_path(w, G.to_dev(d), cap=cap, calls=calls, chunks=2)
+    buf = G.run_path(w, G.to_dev(d), cap=cap, calls=calls)
     o = _oracle(w, d, cap)
     assert o["status"] & ref.ST_CAPACITY
     G.compare_with_oracle(w, buf, o)
