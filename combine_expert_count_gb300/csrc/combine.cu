@@ -120,6 +120,7 @@ cudaError_t launch_combine_reduce(const moe_shape &sh, int cap, const uint16_t *
 // folds the same values into the fp32 accumulator in slot order, as
 // moe_combine_recv would after reading them back.  A row whose grouped
 // position was dropped is written as zeros and contributes w * 0.
+template <int KR>  // 0: slots read from shared memory; else R <= KR slots held in registers
 __global__ void __launch_bounds__(kReduceThreads)
     k_combine_fused(int N, int T, int E, int R, int H, int cap, const uint16_t *__restrict__ y,
                     const int32_t *__restrict__ idx, const float *__restrict__ w,
@@ -155,32 +156,65 @@ __global__ void __launch_bounds__(kReduceThreads)
             wk[k] = __ldg(w + tok * R + k);
         }
         __syncthreads();
-        for (int part = threadIdx.x; part < cpr; part += blockDim.x) {
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int k0 = 0; k0 < R; k0 += kReduceGroup) {
-                uint4 v[kReduceGroup];
+        if constexpr (KR > 0) {
+            const uint4 *ys[KR];
+            uint4 *cs[KR];
+            float wr[KR];
 #pragma unroll
-                for (int u = 0; u < kReduceGroup; ++u) {
-                    const int k = k0 + u;
-                    v[u] = make_uint4(0, 0, 0, 0);
-                    if (k < R && ysrc[k] >= 0)
-                        v[u] = __ldcs(reinterpret_cast<const uint4 *>(y + ysrc[k]) + part);
-                }
+            for (int u = 0; u < KR; ++u) {
+                const bool on = u < R;
+                ys[u] = on && ysrc[u] >= 0 ? reinterpret_cast<const uint4 *>(y + ysrc[u]) : nullptr;
+                cs[u] = on && cdst[u] >= 0 ? reinterpret_cast<uint4 *>(csend + cdst[u]) : nullptr;
+                wr[u] = on ? wk[u] : 0.0f;
+            }
+            for (int part = threadIdx.x; part < cpr; part += blockDim.x) {
+                uint4 v[KR];
 #pragma unroll
-                for (int u = 0; u < kReduceGroup; ++u) {
-                    const int k = k0 + u;
-                    if (k < R && cdst[k] >= 0) {
-                        reinterpret_cast<uint4 *>(csend + cdst[k])[part] = v[u];
-                        fma8(acc, wk[k], v[u]);
+                for (int u = 0; u < KR; ++u)
+                    v[u] = ys[u] ? __ldcs(ys[u] + part) : make_uint4(0, 0, 0, 0);
+                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int u = 0; u < KR; ++u) {
+                    if (cs[u]) {
+                        cs[u][part] = v[u];
+                        fma8(acc, wr[u], v[u]);
                     }
                 }
+                uint4 o;
+                o.x = pack_bf16x2(acc[0], acc[1]);
+                o.y = pack_bf16x2(acc[2], acc[3]);
+                o.z = pack_bf16x2(acc[4], acc[5]);
+                o.w = pack_bf16x2(acc[6], acc[7]);
+                reinterpret_cast<uint4 *>(out + tok * H)[part] = o;
             }
-            uint4 o;
-            o.x = pack_bf16x2(acc[0], acc[1]);
-            o.y = pack_bf16x2(acc[2], acc[3]);
-            o.z = pack_bf16x2(acc[4], acc[5]);
-            o.w = pack_bf16x2(acc[6], acc[7]);
-            reinterpret_cast<uint4 *>(out + tok * H)[part] = o;
+        } else {
+            for (int part = threadIdx.x; part < cpr; part += blockDim.x) {
+                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                for (int k0 = 0; k0 < R; k0 += kReduceGroup) {
+                    uint4 v[kReduceGroup];
+#pragma unroll
+                    for (int u = 0; u < kReduceGroup; ++u) {
+                        const int k = k0 + u;
+                        v[u] = make_uint4(0, 0, 0, 0);
+                        if (k < R && ysrc[k] >= 0)
+                            v[u] = __ldcs(reinterpret_cast<const uint4 *>(y + ysrc[k]) + part);
+                    }
+#pragma unroll
+                    for (int u = 0; u < kReduceGroup; ++u) {
+                        const int k = k0 + u;
+                        if (k < R && cdst[k] >= 0) {
+                            reinterpret_cast<uint4 *>(csend + cdst[k])[part] = v[u];
+                            fma8(acc, wk[k], v[u]);
+                        }
+                    }
+                }
+                uint4 o;
+                o.x = pack_bf16x2(acc[0], acc[1]);
+                o.y = pack_bf16x2(acc[2], acc[3]);
+                o.z = pack_bf16x2(acc[4], acc[5]);
+                o.w = pack_bf16x2(acc[6], acc[7]);
+                reinterpret_cast<uint4 *>(out + tok * H)[part] = o;
+            }
         }
         __syncthreads();
     }
@@ -194,9 +228,10 @@ cudaError_t launch_combine_fused(const moe_shape &sh, int cap, const uint16_t *y
     const long long ntok = (long long)sh.N * sh.T;
     if (ntok <= 0) return cudaSuccess;
     const int grid = (int)(ntok < (1LL << 30) ? ntok : (1LL << 30));
-    return launch_kernel(k_combine_fused, dim3((unsigned)grid), dim3(kReduceThreads), 0, st, sh.N,
-                         sh.T, sh.E, sh.R, sh.H, cap, y, idx, w, slot_row, eso, seg_off, send_off,
-                         csend_off, csend, out);
+    auto kern = sh.R <= 8 ? k_combine_fused<8> : k_combine_fused<0>;
+    return launch_kernel(kern, dim3((unsigned)grid), dim3(kReduceThreads), 0, st, sh.N, sh.T, sh.E,
+                         sh.R, sh.H, cap, y, idx, w, slot_row, eso, seg_off, send_off, csend_off,
+                         csend, out);
 }
 
 // ------------------------------------------------------------ expert stand-in

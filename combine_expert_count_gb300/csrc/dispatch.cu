@@ -139,7 +139,10 @@ __global__ void __launch_bounds__(256)
         const long long s = div_nonneg(tok, T);
         const int t = (int)(tok - s * T);
         if (tid == 0 && item + G < nitems) issue_load(item + G, b ^ 1);
-        if (tid == 0) bulk_wait_read<1>();  // stores of item n-2 are done with buffer b
+        // threads < R issue the stores (one destination each, bulk groups are
+        // per thread): each makes sure its stores of item n-2 are done reading
+        // buffer b before the barrier below lets it be overwritten
+        if (tid < R) bulk_wait_read<1>();
         const bool ok = mbar_wait(&xbar[b], (uint32_t)((n >> 1) & 1));
         if (__syncthreads_or(!ok)) {
             timed_out = true;
@@ -178,16 +181,14 @@ __global__ void __launch_bounds__(256)
         if (tid < R && item + G < nitems)
             dest_rows<kGrouped>(tok0 + div_nonneg(item + G, npieces), tid, T, R, TR, slot_row, gd,
                                 prow, pgrow);
-        if (tid == 0) {
-            for (int k = 0; k < R; ++k) {
-                const long long row = rows[b][k];
-                if (row < 0) continue;
+        if (tid < R) {
+            const long long row = rows[b][tid];
+            if (row >= 0) {
                 bulk_s2g(send_q + row * H + off, qs, (uint32_t)len);
                 if (bulk_scales)
                     bulk_s2g(send_s + row * Sb + (off >> 7), ss, (uint32_t)(len >> 7) * 4u);
-                if (kGrouped) {
-                    const long long grow = grows[b][k];
-                    if (grow < 0) continue;
+                const long long grow = kGrouped ? grows[b][tid] : -1;
+                if (grow >= 0) {
                     bulk_s2g(gd.grp_q + grow * H + off, qs, (uint32_t)len);
                     if (bulk_scales)
                         bulk_s2g(gd.grp_s + grow * Sb + (off >> 7), ss, (uint32_t)(len >> 7) * 4u);
@@ -211,8 +212,8 @@ __global__ void __launch_bounds__(256)
                 *reinterpret_cast<int2 *>(gd.grp_src + grows[b][tid] * 2) = make_int2((int)s, t);
         }
     }
+    if (tid < R) bulk_wait_all();
     if (tid == 0) {
-        bulk_wait_all();
         if (timed_out) {
             flag(status, MOE_ST_TIMEOUT);
             // let the loads of items n and n+1 land before shared memory goes away

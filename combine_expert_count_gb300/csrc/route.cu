@@ -4,12 +4,9 @@
 //
 // k_route_count: one 1024-thread block per rank, as the page describes
 //   (counts accumulated with shared-memory atomics inside a single block,
-//   then a cumulative sum).  The stable slot of every (t, k) is found chunk
-//   by chunk: __match_any_sync gives each lane its rank among equal experts
-//   in its warp, a per-(expert, warp) table scanned across warps gives the
-//   rank among earlier warps of the chunk, and a running count per expert
-//   carries the earlier chunks.  The result equals "expert offset + number of
-//   earlier assignments with the same expert", independent of atomic order.
+//   then a cumulative sum), and the stable slot of every (t, k) (see
+//   route_sender).  The result equals "expert offset + number of earlier
+//   assignments with the same expert", independent of atomic order.
 //
 // k_exchange: one block per receiver; a block scan over the Er*N counts in
 //   (local expert, sender) order gives seg_off / grp_off / m_sizes, and a
@@ -21,8 +18,18 @@ namespace moe {
 
 constexpr int kRouteThreads = 1024;
 
+// Shared memory of the sender role: cnt, base, run ([E] ints each) and a
+// stamped (warp x expert) table of 32-bit entries.
+static size_t route_smem(int E) { return (size_t)E * 3 * sizeof(int) + (size_t)E * 32 * 4; }
+
 // Sender role of rank s = blockIdx.x: counts, scans and stable slots.
-// `smem` holds 4*E ints and an E x 32 u16 table.
+//
+// Stable slots, one chunk of blockDim.x assignments at a time: a lane's rank
+// among equal experts in its warp comes from __match_any_sync; the count of
+// the same expert in earlier warps of the chunk from a (warp x expert)
+// table in which each warp's leader stores (chunk stamp << 16 | count);
+// entries with another chunk's stamp read as zero, so the table is never
+// cleared.  run[e] carries earlier chunks.
 __device__ __forceinline__ void route_sender(int N, int T, int E, int R,
                                              const int32_t *__restrict__ idx,
                                              int32_t *__restrict__ cnt_out,
@@ -30,11 +37,10 @@ __device__ __forceinline__ void route_sender(int N, int T, int E, int R,
                                              int32_t *__restrict__ eso_out,
                                              int32_t *__restrict__ slot_row,
                                              int32_t *__restrict__ status, int *smem) {
-    int *cnt = smem;           // [E] counts
-    int *base = cnt + E;       // [E] exclusive scan of counts
-    int *run = base + E;       // [E] assignments seen in earlier chunks
-    int *ctot = run + E;       // [E] assignments in the current chunk
-    unsigned short *tab = reinterpret_cast<unsigned short *>(ctot + E);  // [E][32]
+    int *cnt = smem;      // [E] counts
+    int *base = cnt + E;  // [E] exclusive scan of counts
+    int *run = base + E;  // [E] assignments seen in earlier chunks
+    uint32_t *tab = reinterpret_cast<uint32_t *>(run + E);  // [32 warps][E]
     __shared__ int wsum[32];
     __shared__ int total;
     __syncthreads();  // callers may reuse shared memory around this
@@ -48,7 +54,7 @@ __device__ __forceinline__ void route_sender(int N, int T, int E, int R,
         cnt[e] = 0;
         run[e] = 0;
     }
-    for (int i = tid; i < E * 32; i += blockDim.x) tab[i] = 0;
+    for (int i = tid; i < nw * E; i += blockDim.x) tab[i] = 0;
     __syncthreads();
 
     // 1. counts with shared-memory atomics
@@ -75,30 +81,46 @@ __device__ __forceinline__ void route_sender(int N, int T, int E, int R,
     for (int p = tid; p <= N; p += blockDim.x)
         send_off[(size_t)s * (N + 1) + p] = p < N ? base[p * Er] : total;
 
-    // 3. stable slots, one chunk of blockDim.x assignments at a time
+    // 3. stable slots
     const unsigned lt = (1u << lane) - 1u;
-    for (int c0 = 0; c0 < TR; c0 += blockDim.x) {
+    for (int c0 = 0, chunk = 0; c0 < TR; c0 += blockDim.x, ++chunk) {
+        const uint32_t stamp = (uint32_t)(chunk % 65535) + 1u;
+        if (chunk > 0 && stamp == 1u) {  // stamps wrap every 65535 chunks: clear once
+            for (int i = tid; i < nw * E; i += blockDim.x) tab[i] = 0;
+            __syncthreads();
+        }
         const int i = c0 + tid;
         const int e = i < TR ? __ldg(id + i) : -1;
         const bool good = (unsigned)e < (unsigned)E;
         const unsigned peers = __match_any_sync(kFull, good ? e : -1);
         const int rank = __popc(peers & lt);
-        if (good && rank == 0) tab[e * 32 + warp] = (unsigned short)__popc(peers);
+        if (good && rank == 0) tab[warp * E + e] = (stamp << 16) | (uint32_t)__popc(peers);
         __syncthreads();
-        for (int x = warp; x < E; x += nw) {
-            int c = lane < nw ? tab[x * 32 + lane] : 0;
-            int ci = warp_inclusive_scan(c);
-            if (lane < nw) tab[x * 32 + lane] = (unsigned short)(ci - c);
-            if (lane == 31) ctot[x] = ci;
+        if (i < TR) {
+            int slot = -1;
+            if (good) {
+                int pre = 0;
+#pragma unroll 8
+                for (int w2 = 0; w2 < warp; ++w2) {
+                    const uint32_t t = tab[w2 * E + e];
+                    pre += (t >> 16) == stamp ? (int)(t & 0xffffu) : 0;
+                }
+                slot = base[e] + run[e] + pre + rank;
+            }
+            slot_row[(size_t)s * TR + i] = slot;
         }
-        __syncthreads();
-        if (i < TR) slot_row[(size_t)s * TR + i] = good ? base[e] + run[e] + tab[e * 32 + warp] + rank : -1;
-        __syncthreads();
-        for (int x = warp; x < E; x += nw) {
-            if (lane < nw) tab[x * 32 + lane] = 0;
-            if (lane == 0) run[x] += ctot[x];
+        if (c0 + (int)blockDim.x < TR) {  // carry this chunk's counts to the next
+            __syncthreads();
+            for (int x = tid; x < E; x += blockDim.x) {
+                int add = 0;
+                for (int w2 = 0; w2 < nw; ++w2) {
+                    const uint32_t t = tab[w2 * E + x];
+                    add += (t >> 16) == stamp ? (int)(t & 0xffffu) : 0;
+                }
+                run[x] += add;
+            }
+            __syncthreads();
         }
-        __syncthreads();
     }
 }
 
@@ -217,8 +239,6 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     route_sender(N, T, E, R, idx, cnt_out, send_off, eso_out, slot_row, status, smem);
 }
 
-static size_t route_smem(int E) { return (size_t)E * 4 * sizeof(int) + (size_t)E * 32 * 2; }
-
 cudaError_t launch_route_count(const moe_shape &sh, const int32_t *idx, int32_t *cnt,
                                int32_t *send_off, int32_t *eso, int32_t *slot_row,
                                int32_t *status, cudaStream_t st) {
@@ -241,6 +261,70 @@ cudaError_t launch_route_count(const moe_shape &sh, const int32_t *idx, int32_t 
     return cudaGetLastError();
 }
 
+// Both roles in one launch with every rank's block in one thread-block
+// cluster: each block plays sender (its counts go to expert_count), all
+// blocks meet at a cluster barrier (release / acquire at cluster scope), and
+// each block then plays receiver, reading the other senders' counts back
+// through L2 -- the routing-information exchange of the pages, between the
+// SMs of one cluster.
+__global__ void __launch_bounds__(kRouteThreads, 1)
+    k_route_cluster(int N, int T, int E, int R, int cap, const int32_t *__restrict__ idx,
+                    int32_t *__restrict__ cnt_out, int32_t *__restrict__ send_off,
+                    int32_t *__restrict__ eso_out, int32_t *__restrict__ slot_row,
+                    int32_t *__restrict__ grp_off, int32_t *__restrict__ seg_off,
+                    int32_t *__restrict__ csend_off, int32_t *__restrict__ m_sizes,
+                    int32_t *__restrict__ status) {
+    extern __shared__ int smem[];
+    route_sender(N, T, E, R, idx, cnt_out, send_off, eso_out, slot_row, status, smem);
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    const int r = blockIdx.x, tid = threadIdx.x, Er = E / N, F = Er * N;
+    const int j = tid / N, s = tid - (tid / N) * N;
+    // written by other blocks in this launch: read through L2, not the read-only path
+    const int v = tid < F ? __ldcg(cnt_out + (size_t)s * E + r * Er + j) : 0;
+    const int w = tid < N ? __ldcg(send_off + (size_t)tid * (N + 1) + r + 1) -
+                                __ldcg(send_off + (size_t)tid * (N + 1) + r)
+                          : 0;
+    route_receiver(N, E, cap, v, w, grp_off, seg_off, csend_off, m_sizes, status);
+}
+
+// Largest cluster k_route_cluster can be launched with on this device (0: none).
+static int route_cluster_limit(int E) {
+    static int cached_dev = -1, cached = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev == cached_dev) return cached;
+    cached_dev = dev;
+    cached = 0;
+    if (cudaFuncSetAttribute(k_route_cluster, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(k_route_cluster, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)route_smem(MOE_MAX_EXPERTS)) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    for (int c = 16; c >= 2; c >>= 1) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(c);
+        cfg.blockDim = dim3(kRouteThreads);
+        cfg.dynamicSmemBytes = route_smem(E);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = c;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, k_route_cluster, &cfg) == cudaSuccess && n >= 1) {
+            cached = c;
+            break;
+        }
+        cudaGetLastError();
+    }
+    return cached;
+}
+
 cudaError_t launch_route(const moe_shape &sh, int cap, const int32_t *idx, int32_t *cnt,
                          int32_t *send_off, int32_t *eso, int32_t *slot_row, int32_t *grp_off,
                          int32_t *seg_off, int32_t *csend_off, int32_t *m_sizes, int32_t *status,
@@ -256,6 +340,23 @@ cudaError_t launch_route(const moe_shape &sh, int cap, const int32_t *idx, int32
                                    (int)route_smem(MOE_MAX_EXPERTS));
         if (err != cudaSuccess) return err;
         attr_dev = dev;
+    }
+    if (sh.N > 1 && sh.N <= route_cluster_limit(sh.E)) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(sh.N);
+        cfg.blockDim = dim3(kRouteThreads);
+        cfg.dynamicSmemBytes = route_smem(sh.E);
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = sh.N;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, k_route_cluster, sh.N, sh.T, sh.E, sh.R, cap, idx, cnt,
+                                  send_off, eso, slot_row, grp_off, seg_off, csend_off, m_sizes,
+                                  status);
     }
     k_route<<<sh.N, kRouteThreads, route_smem(sh.E), st>>>(sh.N, sh.T, sh.E, sh.R, cap, idx, cnt,
                                                          send_off, eso, slot_row, grp_off, seg_off,
