@@ -85,7 +85,9 @@ __device__ __forceinline__ void dest_rows(long long tok, int k, int T, int R, lo
     }
 }
 
-template <bool kGrouped>
+// kHostX: x is pinned host memory, read by the threads with 16-byte loads
+// over the CPU-GPU link (zero copy) instead of by bulk copies.
+template <bool kGrouped, bool kHostX>
 __global__ void __launch_bounds__(256)
     k_quant_pack_staged(int T, int R, int H, int P, long long tok0, long long nitems,
                         const uint16_t *__restrict__ x, const int32_t *__restrict__ slot_row,
@@ -122,7 +124,7 @@ __global__ void __launch_bounds__(256)
     };
 
     const long long first = blockIdx.x, G = gridDim.x;
-    if (tid == 0 && first < nitems) issue_load(first, 0);
+    if (!kHostX && tid == 0 && first < nitems) issue_load(first, 0);
     bool timed_out = false;
     // thread tid < R: destinations of the current item, read one item ahead
     long long prow = -1, pgrow = -1;
@@ -138,15 +140,22 @@ __global__ void __launch_bounds__(256)
         const int off = piece * P, len = min(P, H - off), nch = len >> 4;
         const long long s = div_nonneg(tok, T);
         const int t = (int)(tok - s * T);
-        if (tid == 0 && item + G < nitems) issue_load(item + G, b ^ 1);
+        if (!kHostX && tid == 0 && item + G < nitems) issue_load(item + G, b ^ 1);
         // threads < R issue the stores (one destination each, bulk groups are
         // per thread): each makes sure its stores of item n-2 are done reading
         // buffer b before the barrier below lets it be overwritten
         if (tid < R) bulk_wait_read<1>();
-        const bool ok = mbar_wait(&xbar[b], (uint32_t)((n >> 1) & 1));
-        if (__syncthreads_or(!ok)) {
-            timed_out = true;
-            break;
+        if constexpr (kHostX) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(x + tok * H + off);
+            uint4 *dst = reinterpret_cast<uint4 *>(xbuf + (size_t)b * P);
+            for (int i = tid; i < (len >> 3); i += nthr) dst[i] = src[i];
+            __syncthreads();
+        } else {
+            const bool ok = mbar_wait(&xbar[b], (uint32_t)((n >> 1) & 1));
+            if (__syncthreads_or(!ok)) {
+                timed_out = true;
+                break;
+            }
         }
 
         const uint16_t *xs = xbuf + (size_t)b * P;
@@ -231,13 +240,23 @@ static int quant_threads(int nch) {
     return nch >= 256 ? 256 : 32 * ((nch + 31) / 32);
 }
 
-template <bool kGrouped>
-static cudaError_t launch_staged(const moe_shape &sh, const uint16_t *x, const int32_t *slot_row,
-                                 uint8_t *send_q, float *send_s, int32_t *send_tok,
-                                 int32_t *status, const GroupedDest &gd, cudaStream_t st) {
+// Pinned host memory (reachable from the GPU through unified addressing)?
+static bool is_host_memory(const void *p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeHost;
+}
+
+template <bool kGrouped, bool kHostX>
+static cudaError_t launch_staged_x(const moe_shape &sh, const uint16_t *x,
+                                   const int32_t *slot_row, uint8_t *send_q, float *send_s,
+                                   int32_t *send_tok, int32_t *status, const GroupedDest &gd,
+                                   cudaStream_t st) {
     const long long ntok = (long long)sh.N * sh.T;
-    if (ntok <= 0) return cudaSuccess;
-    auto kern = k_quant_pack_staged<kGrouped>;
+    auto kern = k_quant_pack_staged<kGrouped, kHostX>;
     const int P = sh.H < kPieceElems ? sh.H : kPieceElems;
     const long long nitems = ntok * ((sh.H + P - 1) / P);
     const int threads = quant_threads(P / 16);
@@ -261,6 +280,18 @@ static cudaError_t launch_staged(const moe_shape &sh, const uint16_t *x, const i
     if (grid > nitems) grid = nitems;
     return launch_kernel(kern, dim3((unsigned)grid), dim3(threads), (size_t)smem, st, sh.T, sh.R,
                          sh.H, P, 0LL, nitems, x, slot_row, send_q, send_s, send_tok, status, gd);
+}
+
+template <bool kGrouped>
+static cudaError_t launch_staged(const moe_shape &sh, const uint16_t *x, const int32_t *slot_row,
+                                 uint8_t *send_q, float *send_s, int32_t *send_tok,
+                                 int32_t *status, const GroupedDest &gd, cudaStream_t st) {
+    if ((long long)sh.N * sh.T <= 0) return cudaSuccess;
+    if (is_host_memory(x))
+        return launch_staged_x<kGrouped, true>(sh, x, slot_row, send_q, send_s, send_tok, status,
+                                               gd, st);
+    return launch_staged_x<kGrouped, false>(sh, x, slot_row, send_q, send_s, send_tok, status, gd,
+                                            st);
 }
 
 cudaError_t launch_quant_pack(const moe_shape &sh, const uint16_t *x, const int32_t *slot_row,

@@ -5,7 +5,9 @@ Every function takes torch CUDA tensors (contiguous; raw bytes are what
 counts, so bf16 data may be ``torch.bfloat16`` or any 2-byte dtype, fp8
 payload ``torch.uint8`` or ``torch.float8_e4m3fn``), checks that each buffer
 is large enough for the shape, and passes its device pointer and the current
-torch stream (or ``stream=``) to the library.  All work runs in the library's
+torch stream (or ``stream=``) to the library.  The activations ``x`` and the
+combined output ``out`` may instead be pinned host tensors: the kernels then
+read and write them directly over the CPU-GPU link.  All work runs in the library's
 CUDA kernels; there is no other implementation to fall back on, and importing
 a function without the built library raises.
 
@@ -131,13 +133,19 @@ def sizes_query(shape) -> moe_sizes:
 moe_sizes_query = sizes_query
 
 
+# Buffers that may live in pinned host memory: the kernels read x and write
+# out directly over the CPU-GPU link (zero copy).
+_HOST_OK = ("x", "out", "out_bf16")
+
+
 def _p(t: torch.Tensor | None, nbytes: int, name: str):
     if t is None:
         if nbytes:
             raise ValueError(f"{name}: buffer of {nbytes} bytes required")
         return None
-    if not t.is_cuda:
-        raise ValueError(f"{name}: must be a CUDA tensor")
+    if not t.is_cuda and not (name in _HOST_OK and t.is_pinned()):
+        raise ValueError(f"{name}: must be a CUDA tensor"
+                         + (" or pinned host memory" if name in _HOST_OK else ""))
     if not t.is_contiguous():
         raise ValueError(f"{name}: must be contiguous")
     if t.numel() * t.element_size() < nbytes:

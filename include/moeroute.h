@@ -55,7 +55,9 @@
  *   out             bf16  [N][T][H]     combined output
  *
  * Ownership: every pointer is device memory owned by the caller (sized with
- * moe_sizes_query).  The library allocates nothing and keeps no state
+ * moe_sizes_query), except that x and out may also be pinned host memory
+ * (cudaHostAlloc / page-locked): the kernels then read x and write out
+ * directly over the CPU-GPU link, with no separate copy.  The library allocates nothing and keeps no state
  * between calls.  `stream` is a cudaStream_t (NULL = legacy default stream).
  *
  * Execution: calls only enqueue work on `stream` and never wait for the

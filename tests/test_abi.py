@@ -132,6 +132,19 @@ def test_binding_raises_and_checks_sizes(lib):
                           None, None, None, None, None)
 
 
+@pytest.mark.gpu
+def test_binding_accepts_pinned_host_only_for_x_and_out(lib):
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("pinned host memory needs a CUDA driver")
+    t = torch.zeros(64, dtype=torch.int32).pin_memory()
+    assert m._p(t, 4, "x") is not None
+    with pytest.raises(ValueError):
+        m._p(t, 4, "topk_idx")
+    with pytest.raises(ValueError):
+        m._p(torch.zeros(64, dtype=torch.int32), 4, "x")
+
+
 def test_missing_library_fails_loudly(monkeypatch):
     monkeypatch.setattr(m, "_LIB_PATH", "/nonexistent/libmoeroute.so")
     monkeypatch.setattr(m, "_lib", None)

@@ -79,6 +79,30 @@ def test_fused_and_separate_identical_across_row_pieces(H):
         G.compare_with_oracle(w, G.run_path(w, G.to_dev(d), calls=calls), o)
 
 
+@pytest.mark.parametrize("calls", ["fused", "separate"])
+def test_pinned_host_x_and_out(calls):
+    """x read from, and out written to, pinned host memory by the kernels give
+    the same bytes as device buffers."""
+    w = W.CONFIGS["dsv3_decode"].replace(T=24)
+    d = W.generate(w)
+    dd = G.to_dev(d)
+    ref_buf = G.run_path(w, dd, calls=calls)
+    buf = m.MoeBuffers(w.N, w.T, w.E, w.R, w.H)
+    G.fill_sentinels(buf)
+    xh = torch.empty(dd["x"].shape, dtype=dd["x"].dtype, pin_memory=True)
+    xh.copy_(dd["x"])
+    oh = torch.empty(buf.out.shape, dtype=buf.out.dtype, pin_memory=True)
+    buf.dispatch(xh, dd["topk_idx"], calls=calls)
+    buf.expert(1)
+    buf.combine(dd["topk_idx"], dd["topk_w"], out=oh, calls=calls)
+    torch.cuda.synchronize()
+    assert torch.equal(oh.view(torch.int16), ref_buf.out.cpu().view(torch.int16))
+    n = G.host(ref_buf.grp_off)[:, -1]
+    for r in range(w.N):
+        assert torch.equal(buf.grp_q[r, :n[r]], ref_buf.grp_q[r, :n[r]])
+    assert int(buf.status.item()) == 0
+
+
 def test_worst_case_reduced_t_full_parity():
     """All tokens routed to rank 0's experts, compared in full."""
     w = W.CONFIGS["qwen3_worst"].replace(T=64)
