@@ -19,6 +19,7 @@ dispatch_recv);  ``combine`` = moe_combine (or combine_send, combine_recv).
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 import threading
 
@@ -121,13 +122,23 @@ def _as_shape(shape) -> moe_shape:
     return moe_shape(shape.N, shape.T, shape.E, shape.R, shape.H, int(getattr(shape, "cap", 0)))
 
 
-def sizes_query(shape) -> moe_sizes:
+def _shape_key(sh: moe_shape) -> tuple:
+    return (sh.N, sh.T, sh.E, sh.R, sh.H, sh.cap)
+
+
+@functools.lru_cache(maxsize=256)
+def _sizes_cached(key: tuple) -> moe_sizes:
     out = moe_sizes()
-    sh = _as_shape(shape)
+    sh = moe_shape(*key)
     rc = lib().moe_sizes_query(ctypes.byref(sh), ctypes.byref(out))
     if rc != MOE_OK:
         raise MoeError(rc, "moe_sizes_query")
     return out
+
+
+def sizes_query(shape) -> moe_sizes:
+    """Buffer sizes for a shape (the library's answer, cached per shape)."""
+    return _sizes_cached(_shape_key(_as_shape(shape)))
 
 
 moe_sizes_query = sizes_query
@@ -373,12 +384,25 @@ class MoeBuffers:
         d.update(extra)
         return d
 
+    def _struct(self, need: dict, **inputs) -> moe_buffers:
+        """moe_buffers with this object's buffers (checked once) and the
+        per-call inputs (checked on every call)."""
+        if not hasattr(self, "_b"):
+            self._b = _buffers(self.sizes, self.tensors(), {})  # sized by construction
+        b = moe_buffers.from_buffer_copy(self._b)
+        for name, t in inputs.items():
+            p = _p(t, getattr(self.sizes, need[name]), name)
+            setattr(b, name, p.value if p is not None else None)
+        return b
+
     def dispatch(self, x, topk_idx, stream=None, calls: str = "fused") -> None:
         """The dispatch half.  ``calls``: "fused" (one moe_dispatch call),
         "fused_route" (moe_route then the two dispatch calls) or "separate"
         (the four calls of the pages' steps)."""
         if calls == "fused":
-            moe_dispatch(self.shape, self.tensors(x=x, topk_idx=topk_idx), stream)
+            b = self._struct(_DISPATCH_NEEDS, x=x, topk_idx=topk_idx)
+            _check(lib().moe_dispatch(ctypes.byref(self.shape), ctypes.byref(b), _s(stream)),
+                   "moe_dispatch")
             return
         self.route(topk_idx, stream, calls == "fused_route")
         moe_dispatch_send(self.shape, x, self.slot_row, self.send_q, self.send_s, self.send_tok,
@@ -398,8 +422,10 @@ class MoeBuffers:
         moe_combine_recv."""
         out = self.out if out is None else out
         if calls == "fused":
-            moe_combine(self.shape, self.tensors(topk_idx=topk_idx, topk_w=topk_w,
-                                                 y=self.y if y is None else y, out=out), stream)
+            b = self._struct(_COMBINE_NEEDS, topk_idx=topk_idx, topk_w=topk_w,
+                             y=self.y if y is None else y, out=out)
+            _check(lib().moe_combine(ctypes.byref(self.shape), ctypes.byref(b), _s(stream)),
+                   "moe_combine")
             return out
         moe_combine_send(self.shape, self.y if y is None else y, self.expert_count,
                          self.expert_send_off, self.send_off, self.seg_off, self.csend_off,

@@ -53,3 +53,18 @@ def all_routings(N: int, T: int, E: int, R: int):
     per_token = list(itertools.permutations(range(E), R))
     for combo in itertools.product(per_token, repeat=N * T):
         yield np.array(combo, dtype=np.int32).reshape(N, T, R)
+
+
+def ll_rows(N: int, T: int, E: int, R: int, idx: np.ndarray) -> dict:
+    """Low-latency row of every (s, t, k): region (receiver r, local expert j,
+    sender s) of T rows, position = rank of (t, k) in sorted order among
+    sender s's assignments to that expert; None beyond T rows."""
+    Er = E // N
+    rows = {}
+    for s in range(N):
+        for e in range(E):
+            mine = sorted(a for a in assignments(N, T, E, R, idx) if a[0] == s and a[3] == e)
+            r, j = e // Er, e % Er
+            for u, a in enumerate(mine):
+                rows[a[:3]] = ((r * Er + j) * N + s) * T + u if u < T else None
+    return rows

@@ -488,3 +488,119 @@ void ref_combine_recv(int N, int T, int E, int R, int H, int cap, const uint16_t
     free(rows);
     free(use);
 }
+
+/* ------------------------------------------------------------ low latency */
+
+/* Low-latency layout, after the fixed-size receive buffers of the
+ * low-latency mode the RoCE->EFA page describes (section 4.4: a preset
+ * per-rank token limit, one kernel, no count-then-allocate round):
+ * receiver r keeps, for each local expert j and sender s, a region of T rows.
+ * Assignment (t, k) of sender s with expert e = r*Er + j takes row
+ *   ll_row = ((r*Er + j)*N + s)*T + u,
+ * u = number of earlier (t', k') of rank s, in flattened order, with the same
+ * expert (the same stable order as slot_row).  u >= T cannot happen when a
+ * token's experts are distinct; otherwise the row is dropped (-1) and
+ * REF_ST_CAPACITY is returned.  Bad ids give -1 and REF_ST_BAD_EXPERT.
+ * ll_count[r][j][s] = number of assignments of s to expert r*Er + j. */
+int ref_ll_rows(int N, int T, int E, int R, const int32_t *idx, int32_t *ll_row,
+                int32_t *ll_count)
+{
+    int st = 0;
+    int Er = E / N;
+    int32_t *seen = (int32_t *)calloc((size_t)E, sizeof(int32_t));
+    for (int i = 0; i < N * E; ++i)
+        ll_count[i] = 0;
+    for (int s = 0; s < N; ++s) {
+        for (int e = 0; e < E; ++e)
+            seen[e] = 0;
+        for (int i = 0; i < T * R; ++i) {
+            size_t a = (size_t)s * T * R + i;
+            int e = idx[a];
+            if (e < 0 || e >= E) {
+                ll_row[a] = -1;
+                st |= REF_ST_BAD_EXPERT;
+                continue;
+            }
+            int r = e / Er, j = e % Er;
+            int u = seen[e];
+            seen[e] += 1;
+            ll_count[((size_t)r * Er + j) * N + s] += 1;
+            if (u >= T) {
+                ll_row[a] = -1;
+                st |= REF_ST_CAPACITY;
+                continue;
+            }
+            ll_row[a] = (int32_t)((((size_t)r * Er + j) * N + s) * T + u);
+        }
+    }
+    free(seen);
+    return st;
+}
+
+/* Quantise each token (ref_quant_token) and place its copies at the
+ * low-latency rows, with the source token id beside them. */
+void ref_dispatch_ll(int N, int T, int R, int H, const uint16_t *x, const int32_t *ll_row,
+                     uint8_t *ll_q, float *ll_s, int32_t *ll_src)
+{
+    int Sb = H / 128;
+    uint8_t *q = (uint8_t *)malloc((size_t)H);
+    float *sc = (float *)malloc((size_t)Sb * sizeof(float));
+    for (int s = 0; s < N; ++s) {
+        for (int t = 0; t < T; ++t) {
+            size_t tok = (size_t)s * T + t;
+            ref_quant_token(H, x + tok * H, q, sc);
+            for (int k = 0; k < R; ++k) {
+                int32_t row = ll_row[tok * R + k];
+                if (row < 0)
+                    continue;
+                memcpy(ll_q + (size_t)row * H, q, (size_t)H);
+                memcpy(ll_s + (size_t)row * Sb, sc, (size_t)Sb * sizeof(float));
+                ll_src[row] = t;
+            }
+        }
+    }
+    free(q);
+    free(sc);
+}
+
+/* Stand-in expert over the low-latency layout: rows u < min(count, T) of
+ * every region (r, j, s) of expert e = r*Er + j. */
+void ref_standin_ll(int N, int T, int E, int H, int mode, const uint8_t *ll_q,
+                    const float *ll_s, const int32_t *ll_count, uint16_t *y_ll)
+{
+    int Er = E / N, Sb = H / 128;
+    for (int r = 0; r < N; ++r)
+        for (int j = 0; j < Er; ++j)
+            for (int s = 0; s < N; ++s) {
+                size_t reg = ((size_t)r * Er + j) * N + s;
+                int n = ll_count[reg] < T ? ll_count[reg] : T;
+                for (int u = 0; u < n; ++u) {
+                    size_t row = reg * T + u;
+                    ref_standin_row(H, mode, r * Er + j, ll_q + row * H, ll_s + row * Sb,
+                                    y_ll + row * H);
+                }
+            }
+}
+
+/* Combine over the low-latency layout: token (s, t) reduces its R rows
+ * y_ll[ll_row[s][t][k]] with ref_weighted_sum (dropped rows contribute
+ * nothing). */
+void ref_combine_ll(int N, int T, int R, int H, const uint16_t *y_ll, const float *w,
+                    const int32_t *ll_row, uint16_t *out)
+{
+    uint16_t *rows = (uint16_t *)calloc((size_t)R * H, sizeof(uint16_t));
+    int32_t *use = (int32_t *)calloc((size_t)R, sizeof(int32_t));
+    for (int s = 0; s < N; ++s)
+        for (int t = 0; t < T; ++t) {
+            size_t tok = (size_t)s * T + t;
+            for (int k = 0; k < R; ++k) {
+                int32_t row = ll_row[tok * R + k];
+                use[k] = row >= 0;
+                if (row >= 0)
+                    memcpy(rows + (size_t)k * H, y_ll + (size_t)row * H, (size_t)H * 2);
+            }
+            ref_weighted_sum(R, H, rows, w + tok * R, use, out + tok * H);
+        }
+    free(rows);
+    free(use);
+}

@@ -264,3 +264,47 @@ def layer(N, T, E, R, H, cap, x, topk_idx, topk_w, mode: int = 0) -> dict:
     out["out"] = combine_recv(N, T, E, R, H, cap, out["csend"], topk_idx, topk_w,
                               out["slot_row"], out["send_off"], out["csend_off"])
     return out
+
+
+# ------------------------------------------------------------------ low latency
+
+def ll_rows(N, T, E, R, topk_idx) -> dict:
+    ll_row = np.full((N, T, R), -7, np.int32)
+    ll_count = np.zeros((N, E // N, N), np.int32)
+    st = lib().ref_ll_rows(N, T, E, R, _i32(np.ascontiguousarray(topk_idx, dtype=np.int32)),
+                           _i32(ll_row), _i32(ll_count))
+    return dict(ll_row=ll_row, ll_count=ll_count, status=int(st))
+
+
+def dispatch_ll(N, T, E, R, H, x, ll_row) -> dict:
+    rows = N * E * T
+    ll_q = np.full((rows, H), FILL_U8, np.uint8)
+    ll_s = np.full((rows, H // 128), FILL_F32, np.float32)
+    ll_src = np.full(rows, -1, np.int32)
+    lib().ref_dispatch_ll(N, T, R, H, _u16(np.ascontiguousarray(x, dtype=np.uint16)),
+                          _i32(np.ascontiguousarray(ll_row)), _u8(ll_q), _f32(ll_s), _i32(ll_src))
+    return dict(ll_q=ll_q, ll_s=ll_s, ll_src=ll_src)
+
+
+def standin_ll(N, T, E, H, mode, ll_q, ll_s, ll_count) -> np.ndarray:
+    y = np.full((N * E * T, H), FILL_U16, np.uint16)
+    c = np.ascontiguousarray
+    lib().ref_standin_ll(N, T, E, H, mode, _u8(c(ll_q)), _f32(c(ll_s)), _i32(c(ll_count)), _u16(y))
+    return y
+
+
+def combine_ll(N, T, R, H, y_ll, topk_w, ll_row) -> np.ndarray:
+    out = np.full((N, T, H), FILL_U16, np.uint16)
+    c = np.ascontiguousarray
+    lib().ref_combine_ll(N, T, R, H, _u16(c(y_ll)), _f32(c(topk_w, dtype=np.float32)),
+                         _i32(c(ll_row)), _u16(out))
+    return out
+
+
+def layer_ll(N, T, E, R, H, x, topk_idx, topk_w, mode: int = 0) -> dict:
+    """The low-latency path: rows, dispatch, stand-in, combine."""
+    out = ll_rows(N, T, E, R, topk_idx)
+    out.update(dispatch_ll(N, T, E, R, H, x, out["ll_row"]))
+    out["y_ll"] = standin_ll(N, T, E, H, mode, out["ll_q"], out["ll_s"], out["ll_count"])
+    out["out"] = combine_ll(N, T, R, H, out["y_ll"], topk_w, out["ll_row"])
+    return out

@@ -474,3 +474,51 @@ def test_round_trip_identity_expert(name):
             want = _f32(_bf16(dq.astype(np.float32))).astype(np.float64)
             got = _f32(o["out"][s, t]).astype(np.float64)
             assert np.all(np.abs(got - want) <= np.abs(want) * 2.0 ** -7 + 1e-6)
+
+
+# ----------------------------------------------------------------- low-latency layout
+
+
+def test_ll_rows_bruteforce_all_routings_2x2x4x2():
+    for idx in brute.all_routings(2, 2, 4, 2):
+        o = ref.ll_rows(2, 2, 4, 2, idx)
+        assert o["status"] == 0
+        want = brute.ll_rows(2, 2, 4, 2, idx)
+        for (s, t, k), row in want.items():
+            assert o["ll_row"][s, t, k] == row
+        cnt = np.zeros((2, 2, 2), np.int32)
+        for (s, t, k, e) in brute.assignments(2, 2, 4, 2, idx):
+            cnt[e // 2, e % 2, s] += 1
+        assert np.array_equal(o["ll_count"], cnt)
+
+
+def test_ll_rows_duplicates_overflow_and_bad_ids():
+    N, T, E, R = 2, 2, 4, 3
+    idx = np.array([[[1, 1, 1], [1, 2, 9]], [[0, 3, 2], [-1, 0, 1]]], np.int32)
+    o = ref.ll_rows(N, T, E, R, idx)
+    assert o["status"] == ref.ST_CAPACITY | ref.ST_BAD_EXPERT
+    want = brute.ll_rows(N, T, E, R, idx)
+    for (s, t, k), row in want.items():
+        assert o["ll_row"][s, t, k] == (-1 if row is None else row)
+    assert o["ll_row"][0, 1, 2] == -1 and o["ll_row"][1, 1, 0] == -1
+    assert o["ll_count"][0, 1, 0] == 4   # expert 1 from sender 0: four rows, two fit
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen3_worst"])
+def test_ll_layer_matches_main_path(name):
+    """The low-latency path places the same quantised rows and, with the same
+    slot order of fused multiply-adds, gives the same combined output."""
+    w = W.CONFIGS[name]
+    if name == "qwen3_worst":
+        w = w.replace(T=8, H=256)
+    d = W.generate(w)
+    main = ref.layer(w.N, w.T, w.E, w.R, w.H, w.default_cap, d["x"], d["topk_idx"], d["topk_w"])
+    ll = ref.layer_ll(w.N, w.T, w.E, w.R, w.H, d["x"], d["topk_idx"], d["topk_w"])
+    assert ll["status"] == 0
+    assert np.array_equal(ll["out"], main["out"])
+    for s in range(w.N):
+        for t in range(w.T):
+            for k in range(w.R):
+                row = ll["ll_row"][s, t, k]
+                q, sc = ref.quant_token(w.H, d["x"][s, t])
+                assert np.array_equal(ll["ll_q"][row], q) and ll["ll_src"][row] == t
