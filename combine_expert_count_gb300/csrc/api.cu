@@ -106,6 +106,20 @@ int moe_sizes_query(const moe_shape *sh, moe_sizes *out) {
     out->bytes_grp_s = N * (int64_t)cap * Sb * 4;
     out->bytes_grp_src = N * (int64_t)cap * 8;
     out->bytes_y = N * (int64_t)cap * H * 2;
+    out->ll_rows = N * E * T;
+    out->bytes_ll_q = out->ll_rows * H;
+    out->bytes_ll_s = out->ll_rows * Sb * 4;
+    out->bytes_ll_src = out->ll_rows * 4;
+    out->bytes_ll_count = N * E * 4;
+    out->bytes_ll_y = out->ll_rows * H * 2;
+    return MOE_OK;
+}
+
+// The low-latency calls' extra limits.
+static int check_ll(const moe_shape *sh, moe_sizes *z) {
+    int rc = moe_sizes_query(sh, z);
+    if (rc != MOE_OK) return rc;
+    if (sh->T > 1024 || z->ll_rows >= ((int64_t)1 << 31)) return MOE_ENOTSUP;
     return MOE_OK;
 }
 
@@ -231,6 +245,45 @@ int moe_expert_standin(const moe_shape *sh, int mode, const uint8_t *grp_q, cons
         return MOE_EINVAL;
     return cuda_rc(moe::launch_expert_standin(*sh, (int)z.cap, mode, grp_q, grp_s, grp_off, y_bf16,
                                               as_stream(stream)));
+}
+
+int moe_dispatch_ll(const moe_shape *sh, const uint16_t *x_bf16, const int32_t *topk_idx,
+                    uint8_t *ll_q, float *ll_s, int32_t *ll_src, int32_t *ll_count,
+                    int32_t *ll_row, int32_t *status, void *stream) {
+    moe_sizes z;
+    int rc = check_ll(sh, &z);
+    if (rc != MOE_OK) return rc;
+    if (!ok_ptr(x_bf16, z.bytes_x) || !ok_ptr(topk_idx, z.bytes_topk_idx) ||
+        !ok_ptr(ll_q, z.bytes_ll_q) || !ok_ptr(ll_s, z.bytes_ll_s) ||
+        !ok_ptr(ll_src, z.bytes_ll_src) || !ok_ptr(ll_count, z.bytes_ll_count) ||
+        !ok_ptr(ll_row, z.bytes_topk_idx) || !ok_ptr(status, 4))
+        return MOE_EINVAL;
+    return cuda_rc(moe::launch_dispatch_ll(*sh, x_bf16, topk_idx, ll_q, ll_s, ll_src, ll_count,
+                                           ll_row, status, as_stream(stream)));
+}
+
+int moe_expert_standin_ll(const moe_shape *sh, int mode, const uint8_t *ll_q, const float *ll_s,
+                          const int32_t *ll_count, uint16_t *y_ll, void *stream) {
+    moe_sizes z;
+    int rc = check_ll(sh, &z);
+    if (rc != MOE_OK) return rc;
+    if (mode != 0 && mode != 1) return MOE_EINVAL;
+    if (!ok_ptr(ll_q, z.bytes_ll_q) || !ok_ptr(ll_s, z.bytes_ll_s) ||
+        !ok_ptr(ll_count, z.bytes_ll_count) || !ok_ptr(y_ll, z.bytes_ll_y))
+        return MOE_EINVAL;
+    return cuda_rc(moe::launch_expert_standin_ll(*sh, mode, ll_q, ll_s, ll_count, y_ll,
+                                                 as_stream(stream)));
+}
+
+int moe_combine_ll(const moe_shape *sh, const uint16_t *y_ll, const float *topk_w,
+                   const int32_t *ll_row, uint16_t *out_bf16, int32_t *status, void *stream) {
+    moe_sizes z;
+    int rc = check_ll(sh, &z);
+    if (rc != MOE_OK) return rc;
+    if (!ok_ptr(y_ll, z.bytes_ll_y) || !ok_ptr(topk_w, z.bytes_topk_idx) ||
+        !ok_ptr(ll_row, z.bytes_topk_idx) || !ok_ptr(out_bf16, z.bytes_x) || !ok_ptr(status, 4))
+        return MOE_EINVAL;
+    return cuda_rc(moe::launch_combine_ll(*sh, y_ll, topk_w, ll_row, out_bf16, as_stream(stream)));
 }
 
 int moe_e4m3_encode(const float *v, uint8_t *out, int64_t n, void *stream) {

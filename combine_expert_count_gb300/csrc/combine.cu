@@ -44,12 +44,15 @@ __device__ __forceinline__ void fma8(float (&acc)[8], float w, const uint4 &v) {
     acc[7] = __fmaf_rn(w, bf16_hi(v.w), acc[7]);
 }
 
+// kLL: the rows come from the low-latency layout, row ll_row[s][t][k] of
+// `csend` (there y_ll), instead of the combine send buffers.
+template <bool kLL>
 __global__ void __launch_bounds__(kReduceThreads)
     k_combine_reduce(int N, int T, int E, int R, int H, int cap, long long tok0, long long tok1,
                      const uint16_t *__restrict__ csend, const int32_t *__restrict__ idx,
                      const float *__restrict__ w, const int32_t *__restrict__ slot_row,
                      const int32_t *__restrict__ send_off, const int32_t *__restrict__ csend_off,
-                     uint16_t *__restrict__ out) {
+                     const int32_t *__restrict__ ll_row, uint16_t *__restrict__ out) {
     __shared__ long long src[MOE_MAX_TOPK];  // element offset of row k in csend, -1: skip
     __shared__ float wk[MOE_MAX_TOPK];
     const int Er = E / N, cpr = H >> 3;
@@ -57,14 +60,19 @@ __global__ void __launch_bounds__(kReduceThreads)
         const int s = (int)div_nonneg(tok, T);
         if (threadIdx.x < R) {
             const int k = threadIdx.x;
-            const int e = __ldg(idx + tok * R + k);
-            const int sl = __ldg(slot_row + tok * R + k);
             long long o = -1;
-            if ((unsigned)e < (unsigned)E && sl >= 0) {
-                const int p = e / Er;
-                const int c = __ldg(csend_off + (size_t)p * (N + 1) + s) +
-                              (sl - __ldg(send_off + (size_t)s * (N + 1) + p));
-                if (c >= 0 && c < cap) o = ((long long)p * cap + c) * H;
+            if constexpr (kLL) {
+                const int row = __ldg(ll_row + tok * R + k);
+                if (row >= 0) o = (long long)row * H;
+            } else {
+                const int e = __ldg(idx + tok * R + k);
+                const int sl = __ldg(slot_row + tok * R + k);
+                if ((unsigned)e < (unsigned)E && sl >= 0) {
+                    const int p = e / Er;
+                    const int c = __ldg(csend_off + (size_t)p * (N + 1) + s) +
+                                  (sl - __ldg(send_off + (size_t)s * (N + 1) + p));
+                    if (c >= 0 && c < cap) o = ((long long)p * cap + c) * H;
+                }
             }
             src[k] = o;
             wk[k] = __ldg(w + tok * R + k);
@@ -104,9 +112,20 @@ cudaError_t launch_combine_reduce(const moe_shape &sh, int cap, const uint16_t *
     const long long ntok = (long long)sh.N * sh.T;
     if (ntok <= 0) return cudaSuccess;
     const int grid = (int)(ntok < (1LL << 30) ? ntok : (1LL << 30));
-    return launch_kernel(k_combine_reduce, dim3((unsigned)grid), dim3(kReduceThreads), 0, st,
-                         sh.N, sh.T, sh.E, sh.R, sh.H, cap, 0LL, ntok, csend, idx, w, slot_row,
-                         send_off, csend_off, out);
+    return launch_kernel(k_combine_reduce<false>, dim3((unsigned)grid), dim3(kReduceThreads), 0,
+                         st, sh.N, sh.T, sh.E, sh.R, sh.H, cap, 0LL, ntok, csend, idx, w, slot_row,
+                         send_off, csend_off, (const int32_t *)nullptr, out);
+}
+
+cudaError_t launch_combine_ll(const moe_shape &sh, const uint16_t *y_ll, const float *w,
+                              const int32_t *ll_row, uint16_t *out, cudaStream_t st) {
+    const long long ntok = (long long)sh.N * sh.T;
+    if (ntok <= 0) return cudaSuccess;
+    const int grid = (int)(ntok < (1LL << 30) ? ntok : (1LL << 30));
+    return launch_kernel(k_combine_reduce<true>, dim3((unsigned)grid), dim3(kReduceThreads), 0,
+                         st, sh.N, sh.T, sh.E, sh.R, sh.H, 0, 0LL, ntok, y_ll,
+                         (const int32_t *)nullptr, w, (const int32_t *)nullptr,
+                         (const int32_t *)nullptr, (const int32_t *)nullptr, ll_row, out);
 }
 
 // ------------------------------------------------------------ fused combine
@@ -288,6 +307,57 @@ cudaError_t launch_expert_standin(const moe_shape &sh, int cap, int mode, const 
     const long long cap_blocks = (long long)sm_count() * 8;
     const int grid = (int)(need < cap_blocks ? need : cap_blocks);
     k_expert_standin<<<grid, 256, 0, st>>>(sh.N, sh.E, sh.H, cap, mode, grp_q, grp_s, grp_off, y);
+    return cudaGetLastError();
+}
+
+// Stand-in over the low-latency layout: row `row` is in region
+// reg = row / T = e*N + s (expert e); it holds data when row % T <
+// min(count[reg], T).
+__global__ void __launch_bounds__(256)
+    k_expert_standin_ll(int N, int T, int E, int H, int mode, const uint8_t *__restrict__ ll_q,
+                        const float *__restrict__ ll_s, const int32_t *__restrict__ ll_count,
+                        uint16_t *__restrict__ y) {
+    const int lane = threadIdx.x & 31, Sb = H >> 7;
+    const long long nrows = (long long)N * E * T;
+    const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
+    for (long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+         row < nrows; row += nwarps) {
+        const long long reg = row / T;
+        const int u = (int)(row - reg * T);
+        if (u >= __ldg(ll_count + reg)) continue;
+        const int e = (int)(reg / N);
+        const float se = mode == 0 ? 1.0f : (e % 3 == 0 ? 0.5f : (e % 3 == 1 ? 1.0f : 2.0f));
+        const uint8_t *q = ll_q + row * H;
+        for (int c = lane; c < (H >> 4); c += 32) {
+            const uint4 qv = *reinterpret_cast<const uint4 *>(q + c * 16);
+            const float sc = __ldg(ll_s + row * Sb + (c >> 3));
+            const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+            uint32_t o[8];
+#pragma unroll
+            for (int u2 = 0; u2 < 8; ++u2) {
+                const uint32_t word = qw[u2 >> 1] >> ((u2 & 1) * 16);
+                const float a = __fmul_rn(__fmul_rn(e4m3_to_float((uint8_t)(word & 0xff)), sc), se);
+                const float b =
+                    __fmul_rn(__fmul_rn(e4m3_to_float((uint8_t)((word >> 8) & 0xff)), sc), se);
+                o[u2] = pack_bf16x2(a, b);
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(y + row * H + c * 16);
+            dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+            dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+    }
+}
+
+cudaError_t launch_expert_standin_ll(const moe_shape &sh, int mode, const uint8_t *ll_q,
+                                     const float *ll_s, const int32_t *ll_count, uint16_t *y_ll,
+                                     cudaStream_t st) {
+    const long long nrows = (long long)sh.N * sh.E * sh.T;
+    if (nrows == 0) return cudaSuccess;
+    const long long need = (nrows + 7) / 8;
+    const long long cap_blocks = (long long)sm_count() * 8;
+    const int grid = (int)(need < cap_blocks ? need : cap_blocks);
+    k_expert_standin_ll<<<grid, 256, 0, st>>>(sh.N, sh.T, sh.E, sh.H, mode, ll_q, ll_s, ll_count,
+                                              y_ll);
     return cudaGetLastError();
 }
 

@@ -53,6 +53,20 @@ __device__ __forceinline__ float amax16(const uint4 &a, const uint4 &b) {
     return m;
 }
 
+// Where the quantised rows go: the send buffer (moe_dispatch_send), the send
+// buffer and the grouped layout (fused dispatch), or the low-latency layout.
+enum class Dest { kSend, kSendGrouped, kLowLatency };
+
+// Low-latency layout: receiver r keeps a T-row region per (local expert j,
+// sender s); assignment (t, k) of s with expert e = r*Er + j takes row
+// ((r*Er + j)*N + s)*T + u, u = its stable rank among s's assignments to e.
+struct LLDest {
+    int N, E;
+    const int32_t *idx;
+    int32_t *ll_row;    // [N][T][R] row of each assignment, -1: none
+    int32_t *ll_count;  // [N][Er][N] assignments per region
+};
+
 // Where the grouped copy of each assignment goes, for the fused dispatch:
 // row i = slot of rank s for expert e lands at grouped row
 // seg_off[r][j][s] + (i - expert_send_off[s][e]) of rank r = e / Er.
@@ -87,13 +101,18 @@ __device__ __forceinline__ void dest_rows(long long tok, int k, int T, int R, lo
 
 // kHostX: x is pinned host memory, read by the threads with 16-byte loads
 // over the CPU-GPU link (zero copy) instead of by bulk copies.
-template <bool kGrouped, bool kHostX>
+// kDest == kLowLatency: send_q / send_s / send_tok are the low-latency rows,
+// scales and source ids, and each item's rows are found by the CTA itself
+// (no routing kernel before it).
+template <Dest kDest, bool kHostX>
 __global__ void __launch_bounds__(256)
     k_quant_pack_staged(int T, int R, int H, int P, long long tok0, long long nitems,
                         const uint16_t *__restrict__ x, const int32_t *__restrict__ slot_row,
                         uint8_t *__restrict__ send_q, float *__restrict__ send_s,
                         int32_t *__restrict__ send_tok, int32_t *__restrict__ status,
-                        const GroupedDest gd) {
+                        const GroupedDest gd, const LLDest ll) {
+    constexpr bool kGrouped = kDest == Dest::kSendGrouped;
+    constexpr bool kLL = kDest == Dest::kLowLatency;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     unsigned char *sm = align128(smem_raw);
     uint16_t *xbuf = reinterpret_cast<uint16_t *>(sm);            // [2][P] bf16
@@ -102,6 +121,8 @@ __global__ void __launch_bounds__(256)
     __shared__ uint64_t xbar[2];
     __shared__ long long rows[2][MOE_MAX_TOPK];
     __shared__ long long grows[2][MOE_MAX_TOPK];
+    __shared__ int ek[MOE_MAX_TOPK], uk[MOE_MAX_TOPK];
+    int *hist = reinterpret_cast<int *>(sm + (size_t)6 * P + (size_t)(P >> 7) * 8);  // [E], LL
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthr = blockDim.x;
     const int Sb = H >> 7, npieces = (H + P - 1) / P;
@@ -128,7 +149,7 @@ __global__ void __launch_bounds__(256)
     bool timed_out = false;
     // thread tid < R: destinations of the current item, read one item ahead
     long long prow = -1, pgrow = -1;
-    if (tid < R && first < nitems)
+    if (!kLL && tid < R && first < nitems)
         dest_rows<kGrouped>(tok0 + div_nonneg(first, npieces), tid, T, R, TR, slot_row, gd, prow,
                             pgrow);
 
@@ -141,6 +162,51 @@ __global__ void __launch_bounds__(256)
         const long long s = div_nonneg(tok, T);
         const int t = (int)(tok - s * T);
         if (!kHostX && tid == 0 && item + G < nitems) issue_load(item + G, b ^ 1);
+        if constexpr (kLL) {
+            // rows of this token in the low-latency layout, while x arrives:
+            // u_k = earlier assignments of rank s with the same expert
+            const int32_t *ids = ll.idx + s * TR;
+            if (tid < R) {
+                ek[tid] = __ldg(ll.idx + tok * R + tid);
+                uk[tid] = 0;
+            }
+            __syncthreads();
+            const int lim = t * R + R - 1;
+            for (int i = tid; i < lim; i += nthr) {
+                const int v = __ldg(ids + i);
+                for (int k = 0; k < R; ++k)
+                    if (v == ek[k] && i < t * R + k) atomicAdd(&uk[k], 1);
+            }
+            if (t == 0 && piece == 0) {  // region counts of rank s, once
+                for (int e = tid; e < ll.E; e += nthr) hist[e] = 0;
+                __syncthreads();
+                int bad = 0;
+                for (int i = tid; i < TR; i += nthr) {
+                    const int v = __ldg(ids + i);
+                    if ((unsigned)v < (unsigned)ll.E)
+                        atomicAdd(&hist[v], 1);
+                    else
+                        bad = 1;
+                }
+                if (__syncthreads_or(bad) && tid == 0) flag(status, MOE_ST_BAD_EXPERT);
+                const int Er = ll.E / ll.N;
+                int over = 0;
+                for (int e = tid; e < ll.E; e += nthr) {
+                    ll.ll_count[(size_t)e * ll.N + s] = hist[e];  // region (e / Er, e % Er, s)
+                    over |= hist[e] > T;
+                }
+                (void)Er;
+                if (__syncthreads_or(over) && tid == 0) flag(status, MOE_ST_CAPACITY);
+            }
+            __syncthreads();
+            if (tid < R) {
+                const int e = ek[tid], u = uk[tid];
+                const long long row =
+                    ((unsigned)e < (unsigned)ll.E && u < T) ? ((long long)e * ll.N + s) * T + u : -1;
+                prow = row;
+                if (piece == 0) ll.ll_row[tok * R + tid] = (int32_t)row;
+            }
+        }
         // threads < R issue the stores (one destination each, bulk groups are
         // per thread): each makes sure its stores of item n-2 are done reading
         // buffer b before the barrier below lets it be overwritten
@@ -187,7 +253,7 @@ __global__ void __launch_bounds__(256)
             grows[b][tid] = pgrow;
         }
         __syncthreads();
-        if (tid < R && item + G < nitems)
+        if (!kLL && tid < R && item + G < nitems)
             dest_rows<kGrouped>(tok0 + div_nonneg(item + G, npieces), tid, T, R, TR, slot_row, gd,
                                 prow, pgrow);
         if (tid < R) {
@@ -250,17 +316,18 @@ static bool is_host_memory(const void *p) {
     return a.type == cudaMemoryTypeHost;
 }
 
-template <bool kGrouped, bool kHostX>
+template <Dest kDest, bool kHostX>
 static cudaError_t launch_staged_x(const moe_shape &sh, const uint16_t *x,
                                    const int32_t *slot_row, uint8_t *send_q, float *send_s,
                                    int32_t *send_tok, int32_t *status, const GroupedDest &gd,
-                                   cudaStream_t st) {
+                                   const LLDest &ll, cudaStream_t st) {
     const long long ntok = (long long)sh.N * sh.T;
-    auto kern = k_quant_pack_staged<kGrouped, kHostX>;
+    auto kern = k_quant_pack_staged<kDest, kHostX>;
     const int P = sh.H < kPieceElems ? sh.H : kPieceElems;
     const long long nitems = ntok * ((sh.H + P - 1) / P);
     const int threads = quant_threads(P / 16);
-    const int smem = 6 * P + (P / 128) * 8 + 128;
+    const int smem = 6 * P + (P / 128) * 8 + 128 +
+                     (kDest == Dest::kLowLatency ? MOE_MAX_EXPERTS * 4 : 0);
     static int cached_dev = -1, cached_smem = -1, cached_threads = -1, cached_occ = 1;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -279,26 +346,46 @@ static cudaError_t launch_staged_x(const moe_shape &sh, const uint16_t *x,
     long long grid = (long long)sm_count() * cached_occ;
     if (grid > nitems) grid = nitems;
     return launch_kernel(kern, dim3((unsigned)grid), dim3(threads), (size_t)smem, st, sh.T, sh.R,
-                         sh.H, P, 0LL, nitems, x, slot_row, send_q, send_s, send_tok, status, gd);
+                         sh.H, P, 0LL, nitems, x, slot_row, send_q, send_s, send_tok, status, gd,
+                         ll);
 }
 
-template <bool kGrouped>
+template <Dest kDest>
 static cudaError_t launch_staged(const moe_shape &sh, const uint16_t *x, const int32_t *slot_row,
                                  uint8_t *send_q, float *send_s, int32_t *send_tok,
-                                 int32_t *status, const GroupedDest &gd, cudaStream_t st) {
+                                 int32_t *status, const GroupedDest &gd, const LLDest &ll,
+                                 cudaStream_t st) {
     if ((long long)sh.N * sh.T <= 0) return cudaSuccess;
     if (is_host_memory(x))
-        return launch_staged_x<kGrouped, true>(sh, x, slot_row, send_q, send_s, send_tok, status,
-                                               gd, st);
-    return launch_staged_x<kGrouped, false>(sh, x, slot_row, send_q, send_s, send_tok, status, gd,
-                                            st);
+        return launch_staged_x<kDest, true>(sh, x, slot_row, send_q, send_s, send_tok, status, gd,
+                                            ll, st);
+    return launch_staged_x<kDest, false>(sh, x, slot_row, send_q, send_s, send_tok, status, gd, ll,
+                                         st);
 }
 
 cudaError_t launch_quant_pack(const moe_shape &sh, const uint16_t *x, const int32_t *slot_row,
                               uint8_t *send_q, float *send_s, int32_t *send_tok, int32_t *status,
                               cudaStream_t st) {
     GroupedDest gd = {};
-    return launch_staged<false>(sh, x, slot_row, send_q, send_s, send_tok, status, gd, st);
+    LLDest ll = {};
+    return launch_staged<Dest::kSend>(sh, x, slot_row, send_q, send_s, send_tok, status, gd, ll,
+                                      st);
+}
+
+cudaError_t launch_dispatch_ll(const moe_shape &sh, const uint16_t *x, const int32_t *idx,
+                               uint8_t *ll_q, float *ll_s, int32_t *ll_src, int32_t *ll_count,
+                               int32_t *ll_row, int32_t *status, cudaStream_t st) {
+    cudaError_t err = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
+    if (err != cudaSuccess) return err;
+    GroupedDest gd = {};
+    LLDest ll;
+    ll.N = sh.N;
+    ll.E = sh.E;
+    ll.idx = idx;
+    ll.ll_row = ll_row;
+    ll.ll_count = ll_count;
+    return launch_staged<Dest::kLowLatency>(sh, x, nullptr, ll_q, ll_s, ll_src, status, gd, ll,
+                                            st);
 }
 
 cudaError_t launch_dispatch_fused(const moe_shape &sh, int cap, const uint16_t *x,
@@ -316,7 +403,9 @@ cudaError_t launch_dispatch_fused(const moe_shape &sh, int cap, const uint16_t *
     gd.grp_q = grp_q;
     gd.grp_s = grp_s;
     gd.grp_src = grp_src;
-    return launch_staged<true>(sh, x, slot_row, send_q, send_s, send_tok, status, gd, st);
+    LLDest ll = {};
+    return launch_staged<Dest::kSendGrouped>(sh, x, slot_row, send_q, send_s, send_tok, status, gd,
+                                             ll, st);
 }
 
 }  // namespace moe

@@ -63,6 +63,18 @@ cudaError_t launch_expert_standin(const moe_shape &sh, int cap, int mode, const 
                                   const float *grp_s, const int32_t *grp_off, uint16_t *y,
                                   cudaStream_t st);
 
+// Low-latency layout (fixed T-row region per (local expert, sender)).
+cudaError_t launch_dispatch_ll(const moe_shape &sh, const uint16_t *x, const int32_t *idx,
+                               uint8_t *ll_q, float *ll_s, int32_t *ll_src, int32_t *ll_count,
+                               int32_t *ll_row, int32_t *status, cudaStream_t st);
+
+cudaError_t launch_combine_ll(const moe_shape &sh, const uint16_t *y_ll, const float *w,
+                              const int32_t *ll_row, uint16_t *out, cudaStream_t st);
+
+cudaError_t launch_expert_standin_ll(const moe_shape &sh, int mode, const uint8_t *ll_q,
+                                     const float *ll_s, const int32_t *ll_count, uint16_t *y_ll,
+                                     cudaStream_t st);
+
 cudaError_t launch_e4m3_encode(const float *v, uint8_t *out, int64_t n, cudaStream_t st);
 
 // SM count of the current device (cached per device).

@@ -45,7 +45,8 @@ class moe_shape(ctypes.Structure):
 _SIZE_FIELDS = ("cap", "send_rows", "bytes_x", "bytes_topk_idx", "bytes_expert_count",
                 "bytes_send_off", "bytes_expert_send_off", "bytes_grp_off", "bytes_seg_off",
                 "bytes_m_sizes", "bytes_send_q", "bytes_send_s", "bytes_send_tok", "bytes_grp_q",
-                "bytes_grp_s", "bytes_grp_src", "bytes_y")
+                "bytes_grp_s", "bytes_grp_src", "bytes_y", "ll_rows", "bytes_ll_q",
+                "bytes_ll_s", "bytes_ll_src", "bytes_ll_count", "bytes_ll_y")
 
 
 class moe_sizes(ctypes.Structure):
@@ -95,6 +96,9 @@ def lib() -> ctypes.CDLL:
             h.moe_combine_recv.argtypes = [sp] + [V] * 8 + [V]
             h.moe_expert_standin.argtypes = [sp, I] + [V] * 4 + [V]
             h.moe_e4m3_encode.argtypes = [V, V, ctypes.c_int64, V]
+            h.moe_dispatch_ll.argtypes = [sp] + [V] * 8 + [V]
+            h.moe_expert_standin_ll.argtypes = [sp, I] + [V] * 4 + [V]
+            h.moe_combine_ll.argtypes = [sp] + [V] * 5 + [V]
             h.moe_strerror.argtypes = [I]
             h.moe_strerror.restype = ctypes.c_char_p
             h.moe_version.argtypes = []
@@ -321,6 +325,69 @@ def moe_e4m3_encode(v, out, stream=None) -> None:
     n = v.numel()
     _check(lib().moe_e4m3_encode(_p(v, 4 * n, "v"), _p(out, n, "out"), n, _s(stream)),
            "moe_e4m3_encode")
+
+
+def moe_dispatch_ll(shape, x, topk_idx, ll_q, ll_s, ll_src, ll_count, ll_row, status,
+                    stream=None) -> None:
+    sh, z = _as_shape(shape), sizes_query(shape)
+    _check(lib().moe_dispatch_ll(
+        ctypes.byref(sh), _p(x, z.bytes_x, "x"), _p(topk_idx, z.bytes_topk_idx, "topk_idx"),
+        _p(ll_q, z.bytes_ll_q, "ll_q"), _p(ll_s, z.bytes_ll_s, "ll_s"),
+        _p(ll_src, z.bytes_ll_src, "ll_src"), _p(ll_count, z.bytes_ll_count, "ll_count"),
+        _p(ll_row, z.bytes_topk_idx, "ll_row"), _p(status, 4, "status"), _s(stream)),
+        "moe_dispatch_ll")
+
+
+def moe_expert_standin_ll(shape, mode: int, ll_q, ll_s, ll_count, y_ll, stream=None) -> None:
+    sh, z = _as_shape(shape), sizes_query(shape)
+    _check(lib().moe_expert_standin_ll(
+        ctypes.byref(sh), int(mode), _p(ll_q, z.bytes_ll_q, "ll_q"), _p(ll_s, z.bytes_ll_s, "ll_s"),
+        _p(ll_count, z.bytes_ll_count, "ll_count"), _p(y_ll, z.bytes_ll_y, "y_ll"), _s(stream)),
+        "moe_expert_standin_ll")
+
+
+def moe_combine_ll(shape, y_ll, topk_w, ll_row, out, status, stream=None) -> None:
+    sh, z = _as_shape(shape), sizes_query(shape)
+    _check(lib().moe_combine_ll(
+        ctypes.byref(sh), _p(y_ll, z.bytes_ll_y, "y_ll"), _p(topk_w, z.bytes_topk_idx, "topk_w"),
+        _p(ll_row, z.bytes_topk_idx, "ll_row"), _p(out, z.bytes_x, "out"),
+        _p(status, 4, "status"), _s(stream)),
+        "moe_combine_ll")
+
+
+class MoeLLBuffers:
+    """Device buffers of the low-latency layout for one shape (see
+    include/moeroute.h): ``dispatch`` = moe_dispatch_ll, ``expert`` =
+    moe_expert_standin_ll, ``combine`` = moe_combine_ll."""
+
+    def __init__(self, N: int, T: int, E: int, R: int, H: int,
+                 device: str | torch.device = "cuda"):
+        self.shape = make_shape(N, T, E, R, H)
+        self.sizes = sizes_query(self.shape)
+        self.N, self.T, self.E, self.R, self.H = N, T, E, R, H
+        rows, Er = int(self.sizes.ll_rows), E // N
+        d = torch.device(device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=d)
+        self.ll_q = torch.empty((rows, H), dtype=torch.uint8, device=d)
+        self.ll_s = torch.empty((rows, H // 128), dtype=torch.float32, device=d)
+        self.ll_src = torch.empty(rows, dtype=torch.int32, device=d)
+        self.ll_count = torch.empty((N, Er, N), dtype=torch.int32, device=d)
+        self.ll_row = torch.empty((N, T, R), dtype=torch.int32, device=d)
+        self.y_ll = torch.empty((rows, H), dtype=torch.bfloat16, device=d)
+        self.out = torch.empty((N, T, H), dtype=torch.bfloat16, device=d)
+
+    def dispatch(self, x, topk_idx, stream=None) -> None:
+        moe_dispatch_ll(self.shape, x, topk_idx, self.ll_q, self.ll_s, self.ll_src,
+                        self.ll_count, self.ll_row, self.status, stream)
+
+    def expert(self, mode: int = 0, stream=None) -> None:
+        moe_expert_standin_ll(self.shape, mode, self.ll_q, self.ll_s, self.ll_count, self.y_ll,
+                              stream)
+
+    def combine(self, topk_w, out=None, stream=None) -> torch.Tensor:
+        out = self.out if out is None else out
+        moe_combine_ll(self.shape, self.y_ll, topk_w, self.ll_row, out, self.status, stream)
+        return out
 
 
 class MoeBuffers:

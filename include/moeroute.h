@@ -124,6 +124,14 @@ typedef struct {
     int64_t bytes_grp_s;
     int64_t bytes_grp_src;
     int64_t bytes_y;        /* also bytes_csend */
+    /* low-latency layout (moe_dispatch_ll): a T-row region per (receiver,
+     * local expert, sender), N*E*T rows in all */
+    int64_t ll_rows;
+    int64_t bytes_ll_q;     /* ll_rows * H (fp8) */
+    int64_t bytes_ll_s;     /* ll_rows * H/128 * 4 */
+    int64_t bytes_ll_src;   /* ll_rows * 4 */
+    int64_t bytes_ll_count; /* N*E*4: [N][Er][N] */
+    int64_t bytes_ll_y;     /* ll_rows * H * 2 (bf16 expert outputs) */
 } moe_sizes;
 
 /* Fill *out for *shape.  Host only.  MOE_EINVAL / MOE_ENOTSUP on a bad shape. */
@@ -284,6 +292,45 @@ int moe_dispatch(const moe_shape *shape, const moe_buffers *b, void *stream);
  * topk_w, the routing arrays (from a dispatch of the same topk_idx), csend
  * and out.  Outputs: csend and out, as the two separate calls write them. */
 int moe_combine(const moe_shape *shape, const moe_buffers *b, void *stream);
+
+/* ---------------------------------------------------------------- low latency
+ * Dispatch and combine in one kernel each, for decode-sized batches: the
+ * low-latency mode of the RoCE->EFA page (section 4.4) presets a per-rank
+ * token limit and preallocates fixed receive buffers, so no count-then-
+ * allocate round is needed and the whole dispatch is one kernel that a CUDA
+ * graph can capture.  Here receiver r keeps a T-row region for each local
+ * expert j and sender s:
+ *   ll_q     u8    [N][Er][N][T][H]   row ((r*Er + j)*N + s)*T + u
+ *   ll_s     float [N][Er][N][T][H/128]
+ *   ll_src   int32 [N][Er][N][T]      source token t of each row
+ *   ll_count int32 [N][Er][N]         rows in each region (may exceed T:
+ *                                     the rest are dropped, MOE_ST_CAPACITY)
+ *   ll_row   int32 [N][T][R]          row of each assignment, -1 if none
+ *   y_ll     bf16  [N][Er][N][T][H]   expert outputs in the same rows
+ * where u is the assignment's stable rank among sender s's assignments to
+ * expert e = r*Er + j (the order of slot_row).  No routing exchange, send
+ * buffer or combine send buffer is used: every row's position follows from
+ * the sender's own ids.  Rows past ll_count are left untouched.  Limits: T <=
+ * 1024 (MOE_ENOTSUP beyond), N*E*T < 2^31. */
+
+/* Quantise every token (as moe_dispatch_send) and place its rows, scales and
+ * token id in the low-latency layout; writes ll_row and ll_count.  Clears
+ * *status first; MOE_ST_BAD_EXPERT / MOE_ST_CAPACITY as for the main path. */
+int moe_dispatch_ll(const moe_shape *shape, const uint16_t *x_bf16, const int32_t *topk_idx,
+                    uint8_t *ll_q, float *ll_s, int32_t *ll_src, int32_t *ll_count,
+                    int32_t *ll_row, int32_t *status, void *stream);
+
+/* The grouped-GEMM stand-in of moe_expert_standin over the low-latency
+ * layout (rows u < min(ll_count, T) of each region). */
+int moe_expert_standin_ll(const moe_shape *shape, int mode, const uint8_t *ll_q,
+                          const float *ll_s, const int32_t *ll_count, uint16_t *y_ll,
+                          void *stream);
+
+/* Weighted average of each token's rows y_ll[ll_row[s][t][k]], fp32 FMA in
+ * slot order, one bf16 rounding (as moe_combine_recv).  out may be pinned host
+ * memory. */
+int moe_combine_ll(const moe_shape *shape, const uint16_t *y_ll, const float *topk_w,
+                   const int32_t *ll_row, uint16_t *out_bf16, int32_t *status, void *stream);
 
 /* Static description of an error code or status bit set. */
 const char *moe_strerror(int code);

@@ -68,6 +68,8 @@ def test_sizes_query_matches_layout(lib, name):
     assert z.bytes_grp_q == N * cap * H and z.bytes_grp_s == N * cap * Sb * 4
     assert z.bytes_grp_src == N * cap * 8 and z.bytes_y == N * cap * H * 2
     assert z.bytes_seg_off == N * Er * N * 4 and z.bytes_grp_off == N * (Er + 1) * 4
+    assert z.ll_rows == N * E * T and z.bytes_ll_q == N * E * T * H
+    assert z.bytes_ll_count == N * E * 4 and z.bytes_ll_y == N * E * T * H * 2
     z2 = m.sizes_query(m.make_shape(w.N, w.T, w.E, w.R, w.H, 100))
     assert z2.cap == 100 and z2.bytes_grp_q == N * 100 * H
 
@@ -100,6 +102,7 @@ def test_null_and_misaligned_pointers_rejected(lib):
     calls = {
         "moe_route_count": 6, "moe_exchange": 7, "moe_route": 10, "moe_dispatch_send": 6,
         "moe_dispatch_recv": 10, "moe_combine_send": 8, "moe_combine_recv": 8,
+        "moe_dispatch_ll": 8, "moe_combine_ll": 5,
     }
     for name, nptr in calls.items():
         fn = getattr(L, name)
