@@ -95,9 +95,9 @@ def measured_peak():
 # while these are unchanged.
 KERNEL_SOURCES = {
     "route": ("route.cu", "common.cuh"),
-    "dispatch_fused": ("dispatch.cu", "common.cuh"),
+    "dispatch_fused": ("dispatch.cu", "shuffle.cuh", "common.cuh"),
     "combine_fused": ("combine.cu", "common.cuh"),
-    "dispatch_send": ("dispatch.cu", "common.cuh"),
+    "dispatch_send": ("dispatch.cu", "shuffle.cuh", "common.cuh"),
     "dispatch_recv": ("shuffle.cu", "shuffle.cuh", "common.cuh"),
     "combine_send": ("shuffle.cu", "shuffle.cuh", "common.cuh"),
     "combine_recv": ("combine.cu", "common.cuh"),
@@ -471,7 +471,7 @@ def run_ours(args) -> None:
             if k >= W_:
                 e2e_copy_ms.append(e0.elapsed_time(e1))
 
-    # the low-latency calls (SURVEY NEXT-3) on the same workload, when T fits
+    # the low-latency calls on the same workload, when T fits
     ll = None
     if w.T <= 1024:
         llb = m.MoeLLBuffers(w.N, w.T, w.E, w.R, w.H, device=dev)
@@ -499,6 +499,33 @@ def run_ours(args) -> None:
               "how": "moe_dispatch_ll + moe_combine_ll (fixed T-row regions per (expert, "
                      "sender); no send or combine send buffers), CUDA-graph replay"}
         del llb
+
+    # the signalled dispatch: route, then send and receive shuffle in one
+    # kernel handing rows over by per-(sender, receiver) flags; same outputs
+    # as moe_dispatch, moving the bytes of the separate send + receive
+    buf.dispatch(x, idx, calls="signalled")
+    torch.cuda.synchronize()
+    if int(buf.status.item()) != 0:
+        raise RuntimeError("signalled dispatch raised a status")
+    sig_once = capture(lambda: (buf.dispatch(x, idx, calls="signalled"), buf.combine(idx, wt)))
+    for _ in range(W_):
+        flush.zero_()
+        sig_once()
+    sig_ms = time_steps(sig_once, K)
+    sig_k = time_kernels((route, lambda: buf.dispatch(x, idx, calls="signalled")), K)
+    sig_disp_us = (statistics.mean(sig_k[1]) - statistics.mean(sig_k[0])) * 1000
+    sig_bytes = nbytes["separate"]["dispatch_send"] + nbytes["separate"]["dispatch_recv"]
+    signalled = {
+        "us": round(max_over_ranks(statistics.mean(sig_ms), world) * 1000, 2),
+        "dispatch_call_us": round(statistics.mean(sig_k[1]) * 1000, 2),
+        "kernel_us": round(sig_disp_us, 2),
+        "bytes_moved_mb": round(sig_bytes / 1e6, 1),
+        "achieved_gbs": round(sig_bytes / (sig_disp_us * 1e-6) / 1e9, 1) if sig_disp_us > 0
+        else None,
+        "how": "moe_dispatch_signalled (route + one co-resident kernel: every CTA packs its "
+               "tokens, publishing (sender, receiver) groups, then pulls its send rows as their "
+               "groups are published) + moe_combine, CUDA-graph replay; kernel_us = call minus "
+               "the route kernel"}
 
     mean_step_ms = max_over_ranks(statistics.mean(step_ms), world)
     sep_step_ms = max_over_ranks(statistics.mean(sep_ms), world)
@@ -537,6 +564,7 @@ def run_ours(args) -> None:
         "timing": "CUDA-graph replay" if not args.eager else "eager launches",
         "separate_calls_us": round(sep_step_ms * 1000, 2),
         "low_latency": ll,
+        "signalled": signalled,
         "dispatch_us": round((favg["route"] + favg["dispatch_fused"]) * 1000, 2),
         "combine_us": round(favg["combine_fused"] * 1000, 2),
         "achieved_gbs": round(achieved, 1),

@@ -112,6 +112,7 @@ int moe_sizes_query(const moe_shape *sh, moe_sizes *out) {
     out->bytes_ll_src = out->ll_rows * 4;
     out->bytes_ll_count = N * E * 4;
     out->bytes_ll_y = out->ll_rows * H * 2;
+    out->bytes_sig = (2 * N * N + 4) * 4;
     return MOE_OK;
 }
 

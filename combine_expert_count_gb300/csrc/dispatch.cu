@@ -7,6 +7,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "shuffle.cuh"
 
 namespace moe {
 
@@ -99,18 +100,43 @@ __device__ __forceinline__ void dest_rows(long long tok, int k, int T, int R, lo
     }
 }
 
+// Publication of the send rows by (sender s, receiver r) group, for the
+// signalled dispatch: each (row, piece) written adds one to cnt[s][r] after
+// its bulk store has completed and a release fence; the writer that brings
+// the count to the group's size (rows of s for r, times the pieces per row)
+// fences once more and sets published[s][r] = 1.
+struct Signal {
+    int N, Er, npieces;
+    const int32_t *idx;       // [N][T][R] expert ids
+    const int32_t *send_off;  // [N][N+1] per-peer send offsets
+    int32_t *cnt;             // [N][N] (row, piece) pairs written
+    int32_t *published;       // [N][N] 1 once the group is complete
+};
+
+// Thread k of the CTA publishes its row of an item whose stores completed.
+__device__ __forceinline__ void publish_row(const Signal &sg, int g, int target) {
+    __threadfence();
+    if (atomicAdd(sg.cnt + g, 1) + 1 == target) {
+        __threadfence();
+        st_release(sg.published + g, 1);
+    }
+}
+
 // kHostX: x is pinned host memory, read by the threads with 16-byte loads
 // over the CPU-GPU link (zero copy) instead of by bulk copies.
 // kDest == kLowLatency: send_q / send_s / send_tok are the low-latency rows,
 // scales and source ids, and each item's rows are found by the CTA itself
 // (no routing kernel before it).
-template <Dest kDest, bool kHostX>
-__global__ void __launch_bounds__(256)
-    k_quant_pack_staged(int T, int R, int H, int P, long long tok0, long long nitems,
-                        const uint16_t *__restrict__ x, const int32_t *__restrict__ slot_row,
-                        uint8_t *__restrict__ send_q, float *__restrict__ send_s,
-                        int32_t *__restrict__ send_tok, int32_t *__restrict__ status,
-                        const GroupedDest gd, const LLDest ll) {
+// kSignal: publish every row written (Signal above); a row's group count is
+// bumped two items later, once its bulk stores are known to be complete, and
+// the last two items' rows at the end.
+// The CTA handles items cta, cta + ncta, ...
+template <Dest kDest, bool kHostX, bool kSignal = false>
+__device__ __forceinline__ void quant_pack_body(
+    int T, int R, int H, int P, long long tok0, long long nitems, const uint16_t *__restrict__ x,
+    const int32_t *__restrict__ slot_row, uint8_t *__restrict__ send_q, float *__restrict__ send_s,
+    int32_t *__restrict__ send_tok, int32_t *__restrict__ status, const GroupedDest &gd,
+    const LLDest &ll, const Signal &sg, long long cta, long long ncta) {
     constexpr bool kGrouped = kDest == Dest::kSendGrouped;
     constexpr bool kLL = kDest == Dest::kLowLatency;
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -144,7 +170,10 @@ __global__ void __launch_bounds__(256)
         bulk_g2s(xbuf + (size_t)b * P, x + tok * H + off, (uint32_t)len * 2u, &xbar[b]);
     };
 
-    const long long first = blockIdx.x, G = gridDim.x;
+    const long long first = cta, G = ncta;
+    // kSignal, thread k < R: group and size of its row of items n-2 (old)
+    // and n-1 (new), -1: none
+    int old_g = -1, old_n = 0, new_g = -1, new_n = 0;
     if (!kHostX && tid == 0 && first < nitems) issue_load(first, 0);
     bool timed_out = false;
     // thread tid < R: destinations of the current item, read one item ahead
@@ -210,7 +239,19 @@ __global__ void __launch_bounds__(256)
         // threads < R issue the stores (one destination each, bulk groups are
         // per thread): each makes sure its stores of item n-2 are done reading
         // buffer b before the barrier below lets it be overwritten
-        if (tid < R) bulk_wait_read<1>();
+        if (tid < R) {
+            if constexpr (kSignal) {
+                // item n-2's stores complete: publish its row
+                bulk_wait<1>();
+                fence_proxy_async_global();
+                if (old_g >= 0) publish_row(sg, old_g, old_n);
+                old_g = new_g;
+                old_n = new_n;
+                new_g = -1;
+            } else {
+                bulk_wait_read<1>();
+            }
+        }
         if constexpr (kHostX) {
             const uint4 *src = reinterpret_cast<const uint4 *>(x + tok * H + off);
             uint4 *dst = reinterpret_cast<uint4 *>(xbuf + (size_t)b * P);
@@ -270,6 +311,15 @@ __global__ void __launch_bounds__(256)
                 }
             }
             bulk_commit();
+            if constexpr (kSignal) {
+                const int e = row >= 0 ? __ldg(sg.idx + tok * R + tid) : -1;
+                if ((unsigned)e < (unsigned)(sg.N * sg.Er)) {
+                    const int r = e / sg.Er;
+                    const int32_t *so = sg.send_off + s * (sg.N + 1);
+                    new_g = (int)s * sg.N + r;
+                    new_n = (__ldg(so + r + 1) - __ldg(so + r)) * sg.npieces;
+                }
+            }
         }
         if (!bulk_scales) {
             const int nb = len >> 7;
@@ -288,6 +338,15 @@ __global__ void __launch_bounds__(256)
         }
     }
     if (tid < R) bulk_wait_all();
+    if constexpr (kSignal) {
+        // the last items: their plain stores (ids, scales) precede the barrier
+        if (tid < R) fence_proxy_async_global();
+        __syncthreads();
+        if (tid < R) {
+            if (old_g >= 0) publish_row(sg, old_g, old_n);
+            if (new_g >= 0) publish_row(sg, new_g, new_n);
+        }
+    }
     if (tid == 0) {
         if (timed_out) {
             flag(status, MOE_ST_TIMEOUT);
@@ -296,6 +355,84 @@ __global__ void __launch_bounds__(256)
             if (first + (long long)(n + 1) * G < nitems)
                 mbar_wait(&xbar[(n + 1) & 1], (uint32_t)(((n + 1) >> 1) & 1));
         }
+    }
+}
+
+template <Dest kDest, bool kHostX>
+__global__ void __launch_bounds__(256)
+    k_quant_pack_staged(int T, int R, int H, int P, long long tok0, long long nitems,
+                        const uint16_t *__restrict__ x, const int32_t *__restrict__ slot_row,
+                        uint8_t *__restrict__ send_q, float *__restrict__ send_s,
+                        int32_t *__restrict__ send_tok, int32_t *__restrict__ status,
+                        const GroupedDest gd, const LLDest ll) {
+    const Signal sg = {};
+    quant_pack_body<kDest, kHostX>(T, R, H, P, tok0, nitems, x, slot_row, send_q, send_s,
+                                   send_tok, status, gd, ll, sg, blockIdx.x, gridDim.x);
+}
+
+// ------------------------------------------------------------ signalled dispatch
+//
+// Dispatch send and receive shuffle in one co-resident grid, handing rows
+// over by per-group arrival flags instead of a kernel boundary (the
+// decoupled signalling of "MoE multi-node inference bottleneck overturned:
+// Perseus removes hidden serialization", section 3, Algorithm 1 and
+// Figure 6: transfers first, then one fence and one signal per destination
+// group, issued by whichever participant completes the group).
+// Every CTA first quantises + packs its (token, piece) items into the send
+// buffers (items in order, so senders complete roughly in order), publishing
+// each (sender, receiver) group as its rows complete; then it pulls its
+// contiguous range of send rows into the grouped layout, each row waiting
+// (bounded) until its group is published -- a CTA that finishes packing
+// early starts on the groups already complete while others still pack.
+// The last CTA to finish clears the counters and flags, so the scratch is
+// zero again for the next call.  Registers are capped so that as many CTAs
+// are resident as the shared memory allows (the pull moves 4 vectors per
+// lane per step to stay within the cap).
+#ifndef MOE_SIG_VECS
+#define MOE_SIG_VECS 4
+#endif
+#ifndef MOE_SIG_MINB
+#define MOE_SIG_MINB 4
+#endif
+
+template <bool kHostX>
+__global__ void __launch_bounds__(256, MOE_SIG_MINB)
+    k_dispatch_signalled(int T, int R, int H, int P, long long nitems,
+                         const uint16_t *__restrict__ x, const int32_t *__restrict__ slot_row,
+                         uint8_t *__restrict__ send_q, float *__restrict__ send_s,
+                         int32_t *__restrict__ send_tok, int32_t *__restrict__ status,
+                         const DispatchMapT<true> pull, const Signal sg, int32_t *done) {
+    {
+        const GroupedDest gd = {};
+        const LLDest ll = {};
+        quant_pack_body<Dest::kSend, kHostX, true>(T, R, H, P, 0, nitems, x, slot_row, send_q,
+                                                   send_s, send_tok, status, gd, ll, sg,
+                                                   blockIdx.x, gridDim.x);
+    }
+    {
+        const long long nrows = (long long)pull.N * pull.TR;
+        const int nw = blockDim.x >> 5;
+        const long long W = (long long)gridDim.x * nw;
+        const long long gw = (long long)blockIdx.x * nw + (threadIdx.x >> 5);
+        const long long per = (nrows + W - 1) / W;
+        const long long r0 = gw * per, r1 = min(nrows, r0 + per);
+        if (r0 < r1) copy_rows<MOE_SIG_VECS>(pull, 0, r0, r1);
+    }
+    __shared__ int last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        last = atomicAdd(done, 1) == (int)gridDim.x - 1;
+    }
+    __syncthreads();
+    if (last) {
+        __threadfence();
+        const int n2 = sg.N * sg.N;
+        for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+            sg.cnt[i] = 0;
+            sg.published[i] = 0;
+        }
+        if (threadIdx.x == 0) *done = 0;
     }
 }
 
@@ -386,6 +523,86 @@ cudaError_t launch_dispatch_ll(const moe_shape &sh, const uint16_t *x, const int
     ll.ll_count = ll_count;
     return launch_staged<Dest::kLowLatency>(sh, x, nullptr, ll_q, ll_s, ll_src, status, gd, ll,
                                             st);
+}
+
+template <bool kHostX>
+static cudaError_t launch_signalled_x(const moe_shape &sh, int cap, const uint16_t *x,
+                                      const int32_t *idx, const int32_t *slot_row,
+                                      const int32_t *send_off, const int32_t *eso,
+                                      const int32_t *seg_off, uint8_t *send_q, float *send_s,
+                                      int32_t *send_tok, uint8_t *grp_q, float *grp_s,
+                                      int32_t *grp_src, int32_t *sig, int32_t *status,
+                                      cudaStream_t st) {
+    auto kern = k_dispatch_signalled<kHostX>;
+    const int P = sh.H < kPieceElems ? sh.H : kPieceElems;
+    const int npieces = (sh.H + P - 1) / P;
+    const long long nitems = (long long)sh.N * sh.T * npieces;
+    const int threads = quant_threads(P / 16);
+    const int smem = 6 * P + (P / 128) * 8 + 128;
+    static int cached_dev = -1, cached_smem = -1, cached_threads = -1, cached_occ = 1;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev != cached_dev || smem != cached_smem || threads != cached_threads) {
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (err != cudaSuccess) return err;
+        int occ = 0;
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
+        if (err != cudaSuccess) return err;
+        cached_occ = occ < 1 ? 1 : occ;
+        cached_dev = dev;
+        cached_smem = smem;
+        cached_threads = threads;
+    }
+    // every CTA resident at once: rows wait on groups other CTAs pack
+    long long grid = (long long)sm_count() * cached_occ;
+    if (grid > nitems) grid = nitems;
+    const int N = sh.N;
+    Signal sg;
+    sg.N = N;
+    sg.Er = sh.E / N;
+    sg.npieces = npieces;
+    sg.idx = idx;
+    sg.send_off = send_off;
+    sg.cnt = sig;
+    sg.published = sig + (size_t)N * N;
+    DispatchMapT<true> m;
+    m.N = N;
+    m.E = sh.E;
+    m.Er = sh.E / N;
+    m.Sb = sh.H / 128;
+    m.cap = cap;
+    m.H = sh.H;
+    m.TR = (long long)sh.T * sh.R;
+    m.bulk_scales = (m.Sb % 4) == 0;
+    m.send_q = send_q;
+    m.send_s = send_s;
+    m.send_tok = send_tok;
+    m.eso = eso;
+    m.seg_off = seg_off;
+    m.grp_q = grp_q;
+    m.grp_s = grp_s;
+    m.grp_src = grp_src;
+    m.published = sg.published;
+    m.status = status;
+    return launch_kernel_coresident(kern, dim3((unsigned)grid), dim3(threads), (size_t)smem, st,
+                                    sh.T, sh.R, sh.H, P, nitems, x, slot_row, send_q,
+                                    send_s, send_tok, status, m, sg, sig + 2 * (size_t)N * N);
+}
+
+cudaError_t launch_dispatch_signalled(const moe_shape &sh, int cap, const uint16_t *x,
+                                      const int32_t *idx, const int32_t *slot_row,
+                                      const int32_t *send_off, const int32_t *eso,
+                                      const int32_t *seg_off, uint8_t *send_q, float *send_s,
+                                      int32_t *send_tok, uint8_t *grp_q, float *grp_s,
+                                      int32_t *grp_src, int32_t *sig, int32_t *status,
+                                      cudaStream_t st) {
+    if ((long long)sh.N * sh.T <= 0) return cudaSuccess;
+    if (is_host_memory(x))
+        return launch_signalled_x<true>(sh, cap, x, idx, slot_row, send_off, eso, seg_off, send_q,
+                                        send_s, send_tok, grp_q, grp_s, grp_src, sig, status, st);
+    return launch_signalled_x<false>(sh, cap, x, idx, slot_row, send_off, eso, seg_off, send_q,
+                                     send_s, send_tok, grp_q, grp_s, grp_src, sig, status, st);
 }
 
 cudaError_t launch_dispatch_fused(const moe_shape &sh, int cap, const uint16_t *x,

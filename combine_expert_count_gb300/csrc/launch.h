@@ -35,6 +35,18 @@ cudaError_t launch_dispatch_fused(const moe_shape &sh, int cap, const uint16_t *
                                   int32_t *send_tok, uint8_t *grp_q, float *grp_s,
                                   int32_t *grp_src, int32_t *status, cudaStream_t st);
 
+// Quantise + pack and the receive shuffle in one co-resident grid whose
+// CTAs hand rows over by per-(sender, receiver) arrival flags in `sig`
+// (moe_dispatch_signalled; sig: [N][N] counters, [N][N] flags, one done
+// counter, all zero on entry and on return).
+cudaError_t launch_dispatch_signalled(const moe_shape &sh, int cap, const uint16_t *x,
+                                      const int32_t *idx, const int32_t *slot_row,
+                                      const int32_t *send_off, const int32_t *eso,
+                                      const int32_t *seg_off, uint8_t *send_q, float *send_s,
+                                      int32_t *send_tok, uint8_t *grp_q, float *grp_s,
+                                      int32_t *grp_src, int32_t *sig, int32_t *status,
+                                      cudaStream_t st);
+
 cudaError_t launch_dispatch_pull(const moe_shape &sh, int cap, const uint8_t *send_q,
                                  const float *send_s, const int32_t *send_tok,
                                  const int32_t *eso, const int32_t *seg_off, uint8_t *grp_q,

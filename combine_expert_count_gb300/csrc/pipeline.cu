@@ -15,6 +15,9 @@
 // exchange and then writes its tokens straight to their places ("Send and
 // receive buffers"); with all ranks in one GPU's memory the same knowledge
 // lets the quantiser place each row at its final grouped position.
+// moe_dispatch_signalled: k_route, then the send and the receive shuffle as
+//   two groups of CTAs of one co-resident kernel, handing rows over by
+//   per-(sender, receiver) arrival flags.
 #include <cstdint>
 
 #include "launch.h"
@@ -68,6 +71,25 @@ extern "C" int moe_dispatch(const moe_shape *sh, const moe_buffers *b, void *str
         cudaSuccess)
         return MOE_ECUDA;
     return moe_dispatch_send_recv(sh, b, stream);
+}
+
+extern "C" int moe_dispatch_signalled(const moe_shape *sh, const moe_buffers *b, int32_t *sig,
+                                      void *stream) {
+    moe_sizes z;
+    int rc = check_dispatch(sh, b, z);
+    if (rc != MOE_OK) return rc;
+    if (!aligned(sig, z.bytes_sig)) return MOE_EINVAL;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (moe::launch_route(*sh, (int)z.cap, b->topk_idx, b->expert_count, b->send_off,
+                          b->expert_send_off, b->slot_row, b->grp_off, b->seg_off, b->csend_off,
+                          b->m_sizes, b->status, st) != cudaSuccess)
+        return MOE_ECUDA;
+    if (moe::launch_dispatch_signalled(*sh, (int)z.cap, b->x, b->topk_idx, b->slot_row,
+                                       b->send_off, b->expert_send_off, b->seg_off, b->send_q,
+                                       b->send_s, b->send_tok, b->grp_q, b->grp_s, b->grp_src, sig,
+                                       b->status, st) != cudaSuccess)
+        return MOE_ECUDA;
+    return MOE_OK;
 }
 
 extern "C" int moe_combine(const moe_shape *sh, const moe_buffers *b, void *stream) {

@@ -1,4 +1,5 @@
-// shuffle.cu -- the two row shuffles of the path, both driven by k_row_copy:
+// shuffle.cu -- the two row shuffles of the path, both driven by k_row_copy
+// (the dispatch map and the row routing live in shuffle.cuh):
 //   dispatch receive: send buffers -> expert-grouped layout for the grouped
 //     GEMM ("Enabling trillion-parameter models on AWS EFA", section
 //     "Dispatch and combine": received tokens are shuffled into the tensor
@@ -20,81 +21,12 @@
 
 namespace moe {
 
-// Row i of sender s belongs to expert e (the run of expert_send_off[s] that
-// holds i), hosted by r = e/Er as local expert j; it lands at grouped row
-// seg_off[r][j][s] + (i - expert_send_off[s][e]).  Shared by both maps.
-struct RowRoute {
-    int s, i, r, g;
-    bool valid;
-};
-
-__device__ __forceinline__ RowRoute route_row(long long f, long long TR, int N, int E, int Er,
-                                              const int32_t *__restrict__ eso,
-                                              const int32_t *__restrict__ seg_off) {
-    RowRoute rr;
-    rr.s = (int)div_nonneg(f, TR);
-    rr.i = (int)(f - (long long)rr.s * TR);
-    const int32_t *es = eso + (size_t)rr.s * (E + 1);
-    rr.valid = rr.i < __ldg(es + E);  // beyond the rows s packed: nothing
-    rr.r = 0;
-    rr.g = 0;
-    if (!rr.valid) return rr;
-    const int e = find_run(es, E, rr.i);
-    rr.r = e / Er;
-    const int j = e - rr.r * Er;
-    rr.g = __ldg(seg_off + ((size_t)rr.r * Er + j) * N + rr.s) + (rr.i - __ldg(es + e));
-    return rr;
-}
-
-struct DispatchMap {
-    int N, E, Er, Sb, cap, H;
-    long long TR;
-    bool bulk_scales;  // scale rows are whole 16-byte vectors: move them with the payload
-    const uint8_t *send_q;
-    const float *send_s;
-    const int32_t *send_tok, *eso, *seg_off;
-    uint8_t *grp_q;
-    float *grp_s;
-    int32_t *grp_src;
-
-    __device__ __forceinline__ int vecs_a() const { return H >> 4; }
-    __device__ __forceinline__ int vecs_b() const { return bulk_scales ? Sb >> 2 : 0; }
-
-    __device__ __forceinline__ RowIdx index(long long f) const {
-        const RowRoute rr = route_row(f, TR, N, E, Er, eso, seg_off);
-        RowIdx d = {0, 0, 0};
-        // a grouped row at or past cap is dropped (the exchange flagged it)
-        if (!rr.valid || rr.g < 0 || rr.g >= cap) return d;
-        d.kind = 1;
-        d.src = (long long)rr.s * TR + rr.i;
-        d.dst = (long long)rr.r * cap + rr.g;
-        return d;
-    }
-    __device__ __forceinline__ void side(const RowIdx &d) const {
-        const int s = (int)div_nonneg(d.src, TR);
-        *reinterpret_cast<int2 *>(grp_src + d.dst * 2) = make_int2(s, __ldg(send_tok + d.src));
-        if (!bulk_scales)
-            for (int b = 0; b < Sb; ++b) grp_s[d.dst * Sb + b] = __ldg(send_s + d.src * Sb + b);
-    }
-    __device__ __forceinline__ const uint4 *src_a(long long row) const {
-        return reinterpret_cast<const uint4 *>(send_q + row * H);
-    }
-    __device__ __forceinline__ uint4 *dst_a(long long row) const {
-        return reinterpret_cast<uint4 *>(grp_q + row * H);
-    }
-    __device__ __forceinline__ const uint4 *src_b(long long row) const {
-        return reinterpret_cast<const uint4 *>(send_s + row * Sb);
-    }
-    __device__ __forceinline__ uint4 *dst_b(long long row) const {
-        return reinterpret_cast<uint4 *>(grp_s + row * Sb);
-    }
-};
-
 // The same row (s, i), now for the way back: expert rank r copies its output
 // row (grouped row g) to its combine send buffer at
 // csend_off[r][s] + (i - send_off[s][r]), the position row i has inside the
 // run s sent to r.  If g was dropped for capacity the row is sent as zeros.
 struct CombineMap {
+    static constexpr bool kWaits = false;
     int N, E, Er, cap, H;
     long long TR;
     const uint16_t *y;
@@ -120,7 +52,12 @@ struct CombineMap {
         d.src = (long long)rr.r * cap + rr.g;
         return d;
     }
+    __device__ __forceinline__ void ready(RowIdx &, long long) const {}
     __device__ __forceinline__ void side(const RowIdx &) const {}
+    template <class V>
+    __device__ __forceinline__ V ld(const V *p) const {
+        return __ldcs(p);
+    }
     __device__ __forceinline__ const uint4 *src_a(long long row) const {
         return reinterpret_cast<const uint4 *>(y + row * H);
     }
@@ -179,6 +116,8 @@ cudaError_t launch_dispatch_pull(const moe_shape &sh, int cap, const uint8_t *se
     m.grp_q = grp_q;
     m.grp_s = grp_s;
     m.grp_src = grp_src;
+    m.published = nullptr;
+    m.status = nullptr;
     if (row1 < 0) row1 = (long long)sh.N * m.TR;
     return launch_copy<MOE_DISP_VECS>(m, row0, row1 - row0, st);
 }

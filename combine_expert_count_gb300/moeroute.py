@@ -34,7 +34,9 @@ MOE_ST_BAD_EXPERT, MOE_ST_CAPACITY, MOE_ST_TIMEOUT = 1, 2, 4
 
 EXPORTS = ("moe_sizes_query", "moe_route_count", "moe_exchange", "moe_route", "moe_dispatch_send",
            "moe_dispatch_recv", "moe_combine_send", "moe_combine_recv", "moe_dispatch",
-           "moe_dispatch_send_recv", "moe_combine", "moe_expert_standin", "moe_e4m3_encode", "moe_strerror", "moe_version")
+           "moe_dispatch_send_recv", "moe_dispatch_signalled", "moe_combine", "moe_expert_standin",
+           "moe_e4m3_encode", "moe_dispatch_ll", "moe_expert_standin_ll", "moe_combine_ll",
+           "moe_strerror", "moe_version")
 
 
 class moe_shape(ctypes.Structure):
@@ -46,7 +48,7 @@ _SIZE_FIELDS = ("cap", "send_rows", "bytes_x", "bytes_topk_idx", "bytes_expert_c
                 "bytes_send_off", "bytes_expert_send_off", "bytes_grp_off", "bytes_seg_off",
                 "bytes_m_sizes", "bytes_send_q", "bytes_send_s", "bytes_send_tok", "bytes_grp_q",
                 "bytes_grp_s", "bytes_grp_src", "bytes_y", "ll_rows", "bytes_ll_q",
-                "bytes_ll_s", "bytes_ll_src", "bytes_ll_count", "bytes_ll_y")
+                "bytes_ll_s", "bytes_ll_src", "bytes_ll_count", "bytes_ll_y", "bytes_sig")
 
 
 class moe_sizes(ctypes.Structure):
@@ -89,6 +91,7 @@ def lib() -> ctypes.CDLL:
             h.moe_route.argtypes = [sp] + [V] * 10 + [V]
             h.moe_dispatch.argtypes = [sp, P(moe_buffers), V]
             h.moe_dispatch_send_recv.argtypes = [sp, P(moe_buffers), V]
+            h.moe_dispatch_signalled.argtypes = [sp, P(moe_buffers), V, V]
             h.moe_combine.argtypes = [sp, P(moe_buffers), V]
             h.moe_dispatch_send.argtypes = [sp] + [V] * 6 + [V]
             h.moe_dispatch_recv.argtypes = [sp] + [V] * 10 + [V]
@@ -304,6 +307,17 @@ def moe_dispatch_send_recv(shape, tensors: dict, stream=None) -> None:
            "moe_dispatch_send_recv")
 
 
+def moe_dispatch_signalled(shape, tensors: dict, sig, stream=None) -> None:
+    """Whole dispatch (as moe_dispatch) with the send and the receive shuffle
+    in one kernel that hands rows over by per-(sender, receiver) flags;
+    ``sig`` is the zeroed int32 scratch of ``bytes_sig`` bytes."""
+    sh, z = _as_shape(shape), sizes_query(shape)
+    b = _buffers(z, tensors, _DISPATCH_NEEDS)
+    _check(lib().moe_dispatch_signalled(ctypes.byref(sh), ctypes.byref(b),
+                                        _p(sig, z.bytes_sig, "sig"), _s(stream)),
+           "moe_dispatch_signalled")
+
+
 def moe_combine(shape, tensors: dict, stream=None) -> None:
     """Whole combine in one call; ``tensors`` as for moe_dispatch (y, topk_idx,
     topk_w, routing arrays, csend, out, status)."""
@@ -427,6 +441,8 @@ class MoeBuffers:
         self.y = e((N, cap_, H), torch.bfloat16)
         self.csend = e((N, cap_, H), torch.bfloat16)
         self.out = e((N, T, H), torch.bfloat16)
+        # moe_dispatch_signalled's group counters and flags (zero between calls)
+        self.sig = torch.zeros(int(z.bytes_sig) // 4, dtype=torch.int32, device=d)
 
     def device_bytes(self) -> int:
         return sum(t.numel() * t.element_size() for t in vars(self).values()
@@ -464,12 +480,20 @@ class MoeBuffers:
 
     def dispatch(self, x, topk_idx, stream=None, calls: str = "fused") -> None:
         """The dispatch half.  ``calls``: "fused" (one moe_dispatch call),
-        "fused_route" (moe_route then the two dispatch calls) or "separate"
-        (the four calls of the pages' steps)."""
+        "signalled" (one moe_dispatch_signalled call), "fused_route"
+        (moe_route then the two dispatch calls) or "separate" (the four calls
+        of the pages' steps)."""
         if calls == "fused":
             b = self._struct(_DISPATCH_NEEDS, x=x, topk_idx=topk_idx)
             _check(lib().moe_dispatch(ctypes.byref(self.shape), ctypes.byref(b), _s(stream)),
                    "moe_dispatch")
+            return
+        if calls == "signalled":
+            b = self._struct(_DISPATCH_NEEDS, x=x, topk_idx=topk_idx)
+            _check(lib().moe_dispatch_signalled(ctypes.byref(self.shape), ctypes.byref(b),
+                                                ctypes.c_void_p(self.sig.data_ptr()),
+                                                _s(stream)),
+                   "moe_dispatch_signalled")
             return
         self.route(topk_idx, stream, calls == "fused_route")
         moe_dispatch_send(self.shape, x, self.slot_row, self.send_q, self.send_s, self.send_tok,

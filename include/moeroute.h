@@ -132,6 +132,7 @@ typedef struct {
     int64_t bytes_ll_src;   /* ll_rows * 4 */
     int64_t bytes_ll_count; /* N*E*4: [N][Er][N] */
     int64_t bytes_ll_y;     /* ll_rows * H * 2 (bf16 expert outputs) */
+    int64_t bytes_sig;      /* (2*N*N + 4) * 4: moe_dispatch_signalled's flags */
 } moe_sizes;
 
 /* Fill *out for *shape.  Host only.  MOE_EINVAL / MOE_ENOTSUP on a bad shape. */
@@ -292,6 +293,36 @@ int moe_dispatch(const moe_shape *shape, const moe_buffers *b, void *stream);
  * topk_w, the routing arrays (from a dispatch of the same topk_idx), csend
  * and out.  Outputs: csend and out, as the two separate calls write them. */
 int moe_combine(const moe_shape *shape, const moe_buffers *b, void *stream);
+
+/* ---------------------------------------------------------------- signalled
+ * moe_route, then the dispatch send and the dispatch receive shuffle in ONE
+ * kernel whose parts hand rows over by per-group arrival flags rather than
+ * by a kernel boundary: the one-GPU form of the decoupled signalling of "MoE
+ * multi-node inference bottleneck overturned: Perseus removes hidden
+ * serialization" (section 3, Algorithm 1, Figure 6 -- transfers first, then
+ * one fence and one signal per destination group, set by whichever
+ * participant completes the group).  Packing CTAs quantise and write the
+ * send rows exactly as moe_dispatch_send; each (sender s, receiver r) group
+ * is the run of s's send buffer bound for r (send_off[s][r] ..
+ * send_off[s][r+1]).  Every row written adds one to the group's counter
+ * after its store has completed and a release fence; the writer that
+ * completes the group sets its flag.  Receiving CTAs copy each send row to
+ * its grouped row exactly as moe_dispatch_recv, once the row's group flag is
+ * set, so a receiver starts on sender s while later senders are still being
+ * packed.  Outputs: everything moe_dispatch writes, bit for bit.
+ *
+ * sig: int32 scratch of bytes_sig bytes, caller-owned device memory, 16-byte
+ *   aligned: [N][N] group counters, [N][N] group flags, one completion
+ *   counter.  It must be all zero before the first call; every call leaves it
+ *   zero again (the kernel's last CTA clears it).  Calls that share one sig
+ *   must not overlap in time (the same stream orders them).
+ * Every CTA of the kernel is resident at once (a cooperative launch; it
+ * fails with MOE_ECUDA rather than run partly resident).  Each wait is
+ * bounded (about a second); a group that never completes (a sig that was not
+ * zero) sets MOE_ST_TIMEOUT, its rows are not copied, and the call still
+ * returns and clears sig.  *status is cleared first. */
+int moe_dispatch_signalled(const moe_shape *shape, const moe_buffers *b, int32_t *sig,
+                           void *stream);
 
 /* ---------------------------------------------------------------- low latency
  * Dispatch and combine in one kernel each, for decode-sized batches: the

@@ -45,7 +45,7 @@ def run_path(w: W.Workload, dd: dict, cap: int = 0, mode: int | None = None,
         fill_sentinels(buf)
     buf.dispatch(dd["x"], dd["topk_idx"], calls=calls)
     buf.expert(mode if mode is not None else (1 if w.expert == "scale" else 0))
-    buf.combine(dd["topk_idx"], dd["topk_w"], calls=calls)
+    buf.combine(dd["topk_idx"], dd["topk_w"], calls="fused" if calls == "signalled" else calls)
     torch.cuda.synchronize()
     return buf
 

@@ -70,6 +70,7 @@ def test_sizes_query_matches_layout(lib, name):
     assert z.bytes_seg_off == N * Er * N * 4 and z.bytes_grp_off == N * (Er + 1) * 4
     assert z.ll_rows == N * E * T and z.bytes_ll_q == N * E * T * H
     assert z.bytes_ll_count == N * E * 4 and z.bytes_ll_y == N * E * T * H * 2
+    assert z.bytes_sig == (2 * N * N + 4) * 4
     z2 = m.sizes_query(m.make_shape(w.N, w.T, w.E, w.R, w.H, 100))
     assert z2.cap == 100 and z2.bytes_grp_q == N * 100 * H
 
@@ -118,6 +119,16 @@ def test_null_and_misaligned_pointers_rejected(lib):
             b = m.moe_buffers(*([0x10000] * len(m._BUFFER_FIELDS)))
             setattr(b, field, 0x10004)
             assert fn(ctypes.byref(sh), ctypes.byref(b), None) == m.MOE_EINVAL, field
+    full = m.moe_buffers(*([0x10000] * len(m._BUFFER_FIELDS)))
+    for sig in (bad, null):
+        assert L.moe_dispatch_signalled(ctypes.byref(sh), ctypes.byref(full), sig,
+                                        None) == m.MOE_EINVAL
+    assert L.moe_dispatch_signalled(ctypes.byref(sh), None, good, None) == m.MOE_EINVAL
+    for field in list(m._DISPATCH_NEEDS) + ["status"]:
+        b = m.moe_buffers(*([0x10000] * len(m._BUFFER_FIELDS)))
+        setattr(b, field, 0x10004)
+        assert L.moe_dispatch_signalled(ctypes.byref(sh), ctypes.byref(b), good,
+                                        None) == m.MOE_EINVAL, field
     assert L.moe_expert_standin(ctypes.byref(sh), 2, good, good, good, good, None) == m.MOE_EINVAL
     assert L.moe_expert_standin(ctypes.byref(sh), 0, bad, good, good, good, None) == m.MOE_EINVAL
     assert L.moe_e4m3_encode(null, good, 4, None) == m.MOE_EINVAL
