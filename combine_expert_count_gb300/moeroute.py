@@ -34,7 +34,8 @@ MOE_ST_BAD_EXPERT, MOE_ST_CAPACITY, MOE_ST_TIMEOUT = 1, 2, 4
 
 EXPORTS = ("moe_sizes_query", "moe_route_count", "moe_exchange", "moe_route", "moe_dispatch_send",
            "moe_dispatch_recv", "moe_combine_send", "moe_combine_recv", "moe_dispatch",
-           "moe_dispatch_send_recv", "moe_dispatch_signalled", "moe_combine", "moe_expert_standin",
+           "moe_dispatch_send_recv", "moe_dispatch_signalled", "moe_dispatch_signalled_static",
+           "moe_combine", "moe_expert_standin",
            "moe_e4m3_encode", "moe_dispatch_ll", "moe_expert_standin_ll", "moe_combine_ll",
            "moe_strerror", "moe_version")
 
@@ -92,6 +93,7 @@ def lib() -> ctypes.CDLL:
             h.moe_dispatch.argtypes = [sp, P(moe_buffers), V]
             h.moe_dispatch_send_recv.argtypes = [sp, P(moe_buffers), V]
             h.moe_dispatch_signalled.argtypes = [sp, P(moe_buffers), V, V]
+            h.moe_dispatch_signalled_static.argtypes = [sp, P(moe_buffers), V]
             h.moe_combine.argtypes = [sp, P(moe_buffers), V]
             h.moe_dispatch_send.argtypes = [sp] + [V] * 6 + [V]
             h.moe_dispatch_recv.argtypes = [sp] + [V] * 10 + [V]
@@ -316,6 +318,15 @@ def moe_dispatch_signalled(shape, tensors: dict, sig, stream=None) -> None:
     _check(lib().moe_dispatch_signalled(ctypes.byref(sh), ctypes.byref(b),
                                         _p(sig, z.bytes_sig, "sig"), _s(stream)),
            "moe_dispatch_signalled")
+
+
+def moe_dispatch_signalled_static(shape, tensors: dict, stream=None) -> None:
+    """moe_dispatch_signalled with the library's own static flag scratch (no
+    allocation; N <= 64; calls on one device must not overlap in time)."""
+    sh, z = _as_shape(shape), sizes_query(shape)
+    b = _buffers(z, tensors, _DISPATCH_NEEDS)
+    _check(lib().moe_dispatch_signalled_static(ctypes.byref(sh), ctypes.byref(b), _s(stream)),
+           "moe_dispatch_signalled_static")
 
 
 def moe_combine(shape, tensors: dict, stream=None) -> None:

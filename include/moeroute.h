@@ -324,6 +324,26 @@ int moe_combine(const moe_shape *shape, const moe_buffers *b, void *stream);
 int moe_dispatch_signalled(const moe_shape *shape, const moe_buffers *b, int32_t *sig,
                            void *stream);
 
+/* ---------------------------------------------------------------- no allocation
+ * moe_dispatch_signalled with its flag scratch in a static device array of
+ * this library instead of the caller's sig buffer; the pages have no
+ * counterpart (it is an interface convenience, not a step of the method).
+ * It is for callers that cannot allocate the extra scratch: a serving
+ * process that carves device memory into its own arenas at start-up and
+ * must not allocate while serving, or a C caller that holds only the
+ * moe_buffers set another framework allocated.  The call itself allocates
+ * nothing (no cudaMalloc, no allocating library routine).
+ * Limit: N <= MOE_SIG_STATIC_MAX_N; a larger N returns MOE_ENOTSUP before any
+ * CUDA call.  The first call with a given device current looks up the
+ * array's address on that device (cudaGetSymbolAddress) -- make that first
+ * call before any stream capture.  Each call clears the scratch it uses
+ * (cudaMemsetAsync on `stream`), then does exactly what moe_dispatch_signalled
+ * does.  All calls on one device share the array: calls that overlap in time
+ * (several streams or host threads) race and give wrong results; order them
+ * on one stream. */
+#define MOE_SIG_STATIC_MAX_N 64
+int moe_dispatch_signalled_static(const moe_shape *shape, const moe_buffers *b, void *stream);
+
 /* ---------------------------------------------------------------- low latency
  * Dispatch and combine in one kernel each, for decode-sized batches: the
  * low-latency mode of the RoCE->EFA page (section 4.4) presets a per-rank
