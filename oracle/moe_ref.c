@@ -41,7 +41,11 @@
  *     slot k = 0..R-1 in order, then rounds once to bf16 (nearest even);
  *   - an expert id outside [0, E) is skipped and flagged; a grouped or
  *     combine row at or beyond the capacity is dropped and flagged, and a
- *     dropped assignment contributes zero to the combine.
+ *     dropped assignment contributes zero to the combine;
+ *   - the send-side reduction (an alternative combine, see below) sums a
+ *     token's weighted outputs per expert rank in slot order, rounds that
+ *     partial once to bf16, and the receiver adds the partials in ascending
+ *     rank order in fp32 and rounds once more.
  *
  * Precision: the pages fix fp32 scales, fp8 payload, bf16 outputs and fp32
  * accumulation, so those steps run in exactly those types here.  The
@@ -487,6 +491,96 @@ void ref_combine_recv(int N, int T, int E, int R, int H, int cap, const uint16_t
     }
     free(rows);
     free(use);
+}
+
+/* ------------------------------------------------------------ send-side reduction */
+
+/* Send-side accumulation for the combine: the alternative that the EFA page's
+ * evaluation ("Evaluation: dispatch/combine latency", prefill) contrasts with
+ * its own receive-side-only accumulation -- another implementation sums on
+ * the sending side to cut the bytes transferred, with some risk to accuracy.
+ * On expert rank r, for every token t of every sender s with at least one
+ * assignment to an expert of r (valid id, slot_row >= 0), the weighted
+ * outputs of those experts are summed before they leave r:
+ *   acc = 0;  for k = 0..R-1 in order with e_k / Er == r:
+ *               acc = fma(w_k, y_k, acc)        (y_k = 0 if its grouped row
+ *                                                 was dropped at capacity)
+ *   part[r][s][t] = bf16_rn(acc)
+ * one partial row per (r, s, t) in the fixed layout [N][N][T][H]; the rows of
+ * an (r, s, t) without such an assignment are not written. */
+void ref_combine_partial_send(int N, int T, int E, int R, int H, int cap, const uint16_t *y,
+                              const int32_t *idx, const float *w, const int32_t *slot_row,
+                              const int32_t *expert_send_off, const int32_t *seg_off,
+                              uint16_t *part)
+{
+    int Er = E / N;
+    float *acc = (float *)calloc((size_t)H, sizeof(float));
+    for (int r = 0; r < N; ++r) {
+        for (int s = 0; s < N; ++s) {
+            for (int t = 0; t < T; ++t) {
+                size_t tok = (size_t)s * T + t;
+                int has = 0;
+                for (int h = 0; h < H; ++h)
+                    acc[h] = 0.0f;
+                for (int k = 0; k < R; ++k) {
+                    int e = idx[tok * R + k];
+                    int32_t slot = slot_row[tok * R + k];
+                    if (e < 0 || e >= E || slot < 0 || e / Er != r)
+                        continue;
+                    has = 1;
+                    int j = e - r * Er;
+                    int32_t g = seg_off[((size_t)r * Er + j) * N + s] +
+                                (slot - expert_send_off[(size_t)s * (E + 1) + e]);
+                    if (g >= cap)
+                        continue; /* dropped: the expert output is zero */
+                    const uint16_t *row = y + ((size_t)r * cap + g) * H;
+                    for (int h = 0; h < H; ++h)
+                        acc[h] = fmaf(w[tok * R + k], ref_bf16_to_f32(row[h]), acc[h]);
+                }
+                if (!has)
+                    continue;
+                uint16_t *dst = part + (((size_t)r * N + s) * T + t) * H;
+                for (int h = 0; h < H; ++h)
+                    dst[h] = ref_f32_to_bf16_rn(acc[h]);
+            }
+        }
+    }
+    free(acc);
+}
+
+/* The receiving side of the send-side reduction: token t of rank s adds the
+ * partial rows of the ranks its experts live on, in ascending rank order, in
+ * fp32, and rounds once:
+ *   acc = 0;  for r = 0..N-1 with a partial row:  acc = acc + float(part[r][s][t])
+ *   out[s][t] = bf16_rn(acc)                      (0 for a token with none) */
+void ref_combine_partial_recv(int N, int T, int E, int R, int H, const uint16_t *part,
+                              const int32_t *idx, const int32_t *slot_row, uint16_t *out)
+{
+    int Er = E / N;
+    float *acc = (float *)calloc((size_t)H, sizeof(float));
+    for (int s = 0; s < N; ++s) {
+        for (int t = 0; t < T; ++t) {
+            size_t tok = (size_t)s * T + t;
+            for (int h = 0; h < H; ++h)
+                acc[h] = 0.0f;
+            for (int r = 0; r < N; ++r) {
+                int present = 0;
+                for (int k = 0; k < R; ++k) {
+                    int e = idx[tok * R + k];
+                    if (e >= 0 && e < E && slot_row[tok * R + k] >= 0 && e / Er == r)
+                        present = 1;
+                }
+                if (!present)
+                    continue;
+                const uint16_t *row = part + (((size_t)r * N + s) * T + t) * H;
+                for (int h = 0; h < H; ++h)
+                    acc[h] = acc[h] + ref_bf16_to_f32(row[h]);
+            }
+            for (int h = 0; h < H; ++h)
+                out[tok * H + h] = ref_f32_to_bf16_rn(acc[h]);
+        }
+    }
+    free(acc);
 }
 
 /* ------------------------------------------------------------ low latency */

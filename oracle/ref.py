@@ -74,6 +74,9 @@ _SIGS = {
     "ref_weighted_sum": (None, [_I, _I, _u16p, _f32p, _i32p, _u16p]),
     "ref_combine_recv": (None, [_I, _I, _I, _I, _I, _I, _u16p, _i32p, _f32p, _i32p, _i32p,
                                 _i32p, _u16p]),
+    "ref_combine_partial_send": (None, [_I, _I, _I, _I, _I, _I, _u16p, _i32p, _f32p, _i32p,
+                                        _i32p, _i32p, _u16p]),
+    "ref_combine_partial_recv": (None, [_I, _I, _I, _I, _I, _u16p, _i32p, _i32p, _u16p]),
 }
 
 
@@ -245,6 +248,26 @@ def combine_recv(N, T, E, R, H, cap, csend, topk_idx, topk_w, slot_row, send_off
     return out
 
 
+def combine_partial_send(N, T, E, R, H, cap, y, topk_idx, topk_w, slot_row, expert_send_off,
+                         seg_off) -> np.ndarray:
+    """Send-side reduction: one bf16 partial row per (expert rank, sender,
+    token); rows never written keep the fill pattern."""
+    part = np.full((N, N, T, H), FILL_U16, np.uint16)
+    c = np.ascontiguousarray
+    lib().ref_combine_partial_send(N, T, E, R, H, cap, _u16(c(y)), _i32(c(topk_idx)),
+                                   _f32(c(topk_w, dtype=np.float32)), _i32(c(slot_row)),
+                                   _i32(c(expert_send_off)), _i32(c(seg_off)), _u16(part))
+    return part
+
+
+def combine_partial_recv(N, T, E, R, H, part, topk_idx, slot_row) -> np.ndarray:
+    out = np.full((N, T, H), FILL_U16, np.uint16)
+    c = np.ascontiguousarray
+    lib().ref_combine_partial_recv(N, T, E, R, H, _u16(c(part)), _i32(c(topk_idx)),
+                                   _i32(c(slot_row)), _u16(out))
+    return out
+
+
 # ------------------------------------------------------------------ a whole layer
 
 def layer(N, T, E, R, H, cap, x, topk_idx, topk_w, mode: int = 0) -> dict:
@@ -263,6 +286,17 @@ def layer(N, T, E, R, H, cap, x, topk_idx, topk_w, mode: int = 0) -> dict:
                                 out["csend_off"])
     out["out"] = combine_recv(N, T, E, R, H, cap, out["csend"], topk_idx, topk_w,
                               out["slot_row"], out["send_off"], out["csend_off"])
+    return out
+
+
+def layer_partial(N, T, E, R, H, cap, x, topk_idx, topk_w, mode: int = 0) -> dict:
+    """``layer``, plus the combine with send-side reduction on the same expert
+    outputs: ``part`` (partial rows) and ``out_partial``."""
+    out = layer(N, T, E, R, H, cap, x, topk_idx, topk_w, mode)
+    out["part"] = combine_partial_send(N, T, E, R, H, cap, out["y"], topk_idx, topk_w,
+                                       out["slot_row"], out["expert_send_off"], out["seg_off"])
+    out["out_partial"] = combine_partial_recv(N, T, E, R, H, out["part"], topk_idx,
+                                              out["slot_row"])
     return out
 
 

@@ -23,6 +23,13 @@ What pins each oracle function:
                      identity expert with weights summing to 1.
   ref_weighted_sum   exact rational sum: result within one bf16 step.
   ref_standin_row    exact product in fractions, rounded by torch's bf16 cast.
+  ref_combine_partial_send / _recv (send-side reduction)
+                     exact rational sums on every routing of a tiny shape
+                     and on random shapes with duplicates, bad ids and drops;
+                     hand cases fixing where the per-group rounding happens
+                     and the ascending-rank order of the final sum; one
+                     expert per rank reduces to torch's rounded products; the
+                     two-rounding error bound against the exact sum.
 """
 from __future__ import annotations
 
@@ -522,3 +529,177 @@ def test_ll_layer_matches_main_path(name):
                 row = ll["ll_row"][s, t, k]
                 q, sc = ref.quant_token(w.H, d["x"][s, t])
                 assert np.array_equal(ll["ll_q"][row], q) and ll["ll_src"][row] == t
+
+
+# ----------------------------------------------------------------- send-side reduction
+#
+# ref_combine_partial_send / _recv are pinned by: exact rational sums on
+# every routing of a tiny shape and on random shapes with duplicates, bad ids
+# and capacity drops (values chosen so that every partial and the result are
+# exact in bf16, so any dropped, doubled or mis-weighted term shows); hand
+# cases where the place of the extra bf16 rounding (per rank group) and the
+# order of the final sum (ascending rank) change the result; the set of
+# partial rows written against the brute-force rank sets; and the error
+# bound two bf16 roundings imply, against the exact weighted sum.
+
+
+def _partial_case(N, T, E, R, H, idx, w, yval, cap=None):
+    """Routing arrays from the oracle's pinned route_count / exchange; the
+    expert outputs placed at each assignment's grouped row by the brute-force
+    layout; yval(s, t, k, e) gives the row's H values (exact in bf16)."""
+    cap = cap or N * T * R
+    idx = np.asarray(idx, np.int32).reshape(N, T, R)
+    rc = ref.route_count(N, T, E, R, idx)
+    ex = ref.exchange(N, E, cap, rc["expert_count"], rc["send_off"])
+    _, grp, _ = brute.layouts(N, T, E, R, idx)
+    Er = E // N
+    y = np.zeros((N, cap, H), np.uint16)
+    for (s, t, k), g in grp.items():
+        e = int(idx[s, t, k])
+        if g < cap:
+            y[e // Er, g] = _bf16(np.broadcast_to(np.float32(yval(s, t, k, e)), (H,)))
+    part = ref.combine_partial_send(N, T, E, R, H, cap, y, idx, np.asarray(w, np.float32),
+                                    rc["slot_row"], rc["expert_send_off"], ex["seg_off"])
+    out = ref.combine_partial_recv(N, T, E, R, H, part, idx, rc["slot_row"])
+    return dict(rc=rc, ex=ex, y=y, part=part, out=out, grp=grp, cap=cap, idx=idx)
+
+
+def _rank_sets(N, T, E, R, idx):
+    Er = E // N
+    D = {}
+    for (s, t, k, e) in brute.assignments(N, T, E, R, idx):
+        D.setdefault((s, t), set()).add(e // Er)
+    return D
+
+
+def _check_exact(N, T, E, R, H, idx, w, yv, cap=None):
+    c = _partial_case(N, T, E, R, H, idx, w, lambda s, t, k, e: yv[s, t, k], cap)
+    Er, D = E // N, _rank_sets(N, T, E, R, c["idx"])
+    w = np.asarray(w, np.float32).reshape(N, T, R)
+    for s in range(N):
+        for t in range(T):
+            total = Fraction(0)
+            for r in range(N):
+                got = c["part"][r, s, t]
+                if r not in D.get((s, t), set()):
+                    assert np.all(got == ref.FILL_U16), ("row written", r, s, t)
+                    continue
+                grp_sum = Fraction(0)
+                for k in range(R):
+                    e = int(c["idx"][s, t, k])
+                    if 0 <= e < E and e // Er == r and c["grp"][(s, t, k)] < c["cap"]:
+                        grp_sum += Fraction(float(w[s, t, k])) * Fraction(float(yv[s, t, k]))
+                assert np.all(_f32(got) == float(grp_sum)), (r, s, t)
+                total += grp_sum
+            assert np.all(_f32(c["out"][s, t]) == float(total)), (s, t)
+    return c
+
+
+def test_partial_exact_sums_every_routing_2x2x4x2():
+    rng = np.random.default_rng(31)
+    for idx in brute.all_routings(2, 2, 4, 2):
+        w = rng.choice([0.5, 1.0], size=(2, 2, 2))
+        yv = rng.integers(-3, 4, size=(2, 2, 2)) / 4.0
+        _check_exact(2, 2, 4, 2, 8, idx, w, yv)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_partial_exact_sums_duplicates_bad_ids_and_drops(seed):
+    rng = np.random.default_rng(100 + seed)
+    N = int(rng.integers(1, 5))
+    Er = int(rng.integers(1, 4))
+    E, T, R, H = N * Er, int(rng.integers(1, 6)), int(rng.integers(1, 5)), 8
+    idx = rng.integers(-1, E + 1, size=(N, T, R))     # duplicates and bad ids allowed
+    w = rng.choice([0.5, 1.0], size=(N, T, R))
+    yv = rng.integers(-3, 4, size=(N, T, R)) / 4.0
+    cap = int(rng.integers(1, N * T * R + 1))         # some grouped rows dropped
+    _check_exact(N, T, E, R, H, idx, w, yv, cap)
+
+
+def test_partial_rounds_once_per_rank_group():
+    """Two experts on rank 0 (outputs 1 and 2^-8) and one on rank 1 (2^-8):
+    the rank-0 partial 1 + 2^-8 is a bf16 tie and rounds to 1, then
+    1 + 2^-8 rounds to 1 again; accumulating all three on the receiving side
+    gives 1 + 2^-7 instead."""
+    N, T, E, R, H = 2, 1, 4, 3, 8
+    idx = np.array([[[2, 0, 1]], [[3, 2, 1]]])
+    vals = {0: 1.0, 1: 2.0 ** -8, 2: 2.0 ** -8, 3: 0.5}
+    c = _partial_case(N, T, E, R, H, idx, np.ones((N, T, R)), lambda s, t, k, e: vals[e])
+    assert np.all(_f32(c["part"][0, 0, 0]) == 1.0)
+    assert np.all(_f32(c["part"][1, 0, 0]) == 2.0 ** -8)
+    assert np.all(_f32(c["out"][0, 0]) == 1.0)
+    main = ref.combine_recv(N, T, E, R, H, c["cap"],
+                            ref.combine_send(N, T, E, R, H, c["cap"], c["y"],
+                                             c["rc"]["expert_count"], c["rc"]["expert_send_off"],
+                                             c["rc"]["send_off"], c["ex"]["seg_off"],
+                                             c["ex"]["csend_off"]),
+                            idx, np.ones((N, T, R), np.float32), c["rc"]["slot_row"],
+                            c["rc"]["send_off"], c["ex"]["csend_off"])
+    assert np.all(_f32(main[0, 0]) == 1.0 + 2.0 ** -7)
+
+
+def test_partial_final_sum_in_ascending_rank_order():
+    """Partials 1, 3*2^-24 and -1 on ranks 0, 1, 2 (slots in the order 2, 0,
+    1): in ascending rank order 1 + 3*2^-24 is an fp32 tie that rounds up to
+    1 + 2^-22, leaving 2^-22 after -1; in slot order the result would be
+    3*2^-24."""
+    N, T, E, R, H = 3, 1, 3, 3, 8
+    idx = np.array([[[2, 0, 1]], [[0, 1, 2]], [[1, 2, 0]]])
+    vals = {0: 1.0, 1: 3 * 2.0 ** -24, 2: -1.0}
+    c = _partial_case(N, T, E, R, H, idx, np.ones((N, T, R)), lambda s, t, k, e: vals[e])
+    for s in range(N):
+        assert np.all(_f32(c["out"][s, 0]) == 2.0 ** -22), s
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen3_skew"])
+def test_partial_error_bound_against_exact(name):
+    """|out - X| <= 2^-7 * sum_k |w_k y_k| + 2^-126, X the exact weighted sum:
+    one bf16 rounding per partial and one at the end (unit roundoff 2^-8
+    each), fp32 additions far below that."""
+    w = W.CONFIGS[name]
+    if name == "qwen3_skew":
+        w = w.replace(T=4, H=256)
+    d = W.generate(w)
+    o = ref.layer_partial(w.N, w.T, w.E, w.R, w.H, w.default_cap, d["x"], d["topk_idx"],
+                          d["topk_w"], mode=1)
+    _, grp, _ = brute.layouts(w.N, w.T, w.E, w.R, d["topk_idx"])
+    Er = w.E // w.N
+    worst = 0.0
+    for s in range(w.N):
+        for t in range(w.T):
+            X = np.zeros(w.H)
+            A = np.zeros(w.H)
+            for k in range(w.R):
+                e = int(d["topk_idx"][s, t, k])
+                yk = _f32(o["y"][e // Er, grp[(s, t, k)]]).astype(np.float64)
+                X += float(d["topk_w"][s, t, k]) * yk
+                A += abs(float(d["topk_w"][s, t, k])) * np.abs(yk)
+            err = np.abs(_f32(o["out_partial"][s, t]).astype(np.float64) - X)
+            assert np.all(err <= A * 2.0 ** -7 + 2.0 ** -126)
+            worst = max(worst, float(np.max(err / (A + 1e-30))))
+    assert worst > 0.0  # the extra rounding is visible somewhere
+
+
+def test_partial_one_expert_per_rank_reduces_to_products():
+    """E == N: every rank group holds one assignment, so each partial is the
+    fp32 product w*y rounded to bf16 (torch's casts) and the result is their
+    sum in ascending rank order."""
+    N, T, R, H = 4, 3, 3, 16
+    rng = np.random.default_rng(5)
+    idx = np.stack([np.stack([rng.permutation(N)[:R] for _ in range(T)]) for _ in range(N)])
+    w = rng.random((N, T, R)).astype(np.float32)
+    yv = _f32(_bf16(rng.standard_normal((N, T, R))))
+    c = _partial_case(N, T, N, R, H, idx, w, lambda s, t, k, e: yv[s, t, k])
+    for s in range(N):
+        for t in range(T):
+            acc = np.float32(0.0)
+            for r in range(N):
+                ks = [k for k in range(R) if idx[s, t, k] == r]
+                if not ks:
+                    continue
+                p = (torch.tensor(w[s, t, ks[0]]) * torch.tensor(yv[s, t, ks[0]])).to(
+                    torch.bfloat16).float().item()
+                assert np.all(_f32(c["part"][r, s, t]) == p)
+                acc = np.float32(acc + np.float32(p))
+            want = torch.tensor(float(acc), dtype=torch.float32).to(torch.bfloat16).float().item()
+            assert np.all(_f32(c["out"][s, t]) == want)
