@@ -298,6 +298,80 @@ def run_reference(args) -> None:
     print(json.dumps(line), flush=True)
 
 
+def pairs_of(w, idx) -> int:
+    """(token, expert rank) pairs: the rows the send-side reduction sends."""
+    ranks = np.asarray(idx).reshape(w.N * w.T, w.R) // w.Er
+    return int(sum(len(set(r.tolist())) for r in ranks))
+
+
+def partial_combine_line(m, buf, w, d, x, idx, wt, tens, capture, time_steps, time_kernels,
+                         flush, K, W_, world):
+    """moe_combine_partial timed beside moe_combine on the same step."""
+    import torch
+    buf.combine(idx, wt, calls="partial")
+    torch.cuda.synchronize()
+    once = capture(lambda: (m.moe_dispatch(buf.shape, tens), buf.combine(idx, wt,
+                                                                          calls="partial")))
+    for _ in range(W_):
+        flush.zero_()
+        once()
+    step_ms = time_steps(once, K)
+    kern = time_kernels((lambda: buf.combine(idx, wt, calls="partial"),), K)[0]
+    A = int(buf.send_off[:, -1].sum().item())
+    pairs = pairs_of(w, d["topk_idx"])
+    nbytes = A * 2 * w.H + pairs * 2 * w.H + 2 * w.N * w.T * w.H + 12 * A
+    k_us = statistics.mean(kern) * 1000
+    return {"us": round(max_over_ranks(statistics.mean(step_ms), world) * 1000, 2),
+            "combine_kernel_us": round(k_us, 2),
+            "rows_sent": pairs, "rows_sent_receive_side": A,
+            "bytes_moved_mb": round(nbytes / 1e6, 1),
+            "achieved_gbs": round(nbytes / (k_us * 1e-6) / 1e9, 1),
+            "how": "moe_dispatch + moe_combine_partial (per token, one bf16 partial row per "
+                   "expert rank summed on the sending side, then added on the receiving side), "
+                   "CUDA-graph replay; combine_kernel_us alone"}
+
+
+def skew_line(m, W, name, dev, capture, flush, K, W_) -> dict:
+    """One layer (moe_dispatch + moe_combine, and with moe_combine_partial) on
+    a skewed-routing workload."""
+    import torch
+    w = W.CONFIGS[name]
+    d = W.generate(w)
+    b = m.MoeBuffers(w.N, w.T, w.E, w.R, w.H, device=dev)
+    x = torch.from_numpy(d["x"].view(np.int16)).to(dev)
+    idx = torch.from_numpy(d["topk_idx"]).to(dev)
+    wt = torch.from_numpy(d["topk_w"]).to(dev)
+    b.dispatch(x, idx)
+    b.expert(1 if w.expert == "scale" else 0)
+    b.combine(idx, wt)
+    torch.cuda.synchronize()
+    if int(b.status.item()) != 0:
+        raise RuntimeError(f"{name}: device status {int(b.status.item())}")
+    res = {"workload": name, "max_recv_rows": int(b.grp_off[:, -1].max().item()),
+           "mean_recv_rows": round(float(b.grp_off[:, -1].float().mean().item()), 1)}
+    st = torch.cuda.current_stream()
+    for key, calls in (("us", "fused"), ("us_send_side_reduction", "partial")):
+        once = capture(lambda: (b.dispatch(x, idx), b.combine(idx, wt, calls=calls)))
+        for _ in range(W_):
+            flush.zero_()
+            once()
+        tt = []
+        for _ in range(K):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            once()
+            e1.record(st)
+            tt.append((e0, e1))
+        torch.cuda.synchronize()
+        res[key] = round(statistics.mean(a.elapsed_time(c) for a, c in tt) * 1000, 2)
+    res["rows_sent_send_side"] = pairs_of(w, d["topk_idx"])
+    res["rows_sent_receive_side"] = int(b.send_off[:, -1].sum().item())
+    del b
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args) -> None:
     import torch
 
@@ -527,6 +601,16 @@ def run_ours(args) -> None:
                "groups are published) + moe_combine, CUDA-graph replay; kernel_us = call minus "
                "the route kernel"}
 
+    # the combine with send-side reduction on the same expert outputs
+    partial = partial_combine_line(m, buf, w, d, x, idx, wt, tens, capture, time_steps,
+                                   time_kernels, flush, K, W_, world)
+    if rank == 0 and not args.no_skew:
+        skew = [skew_line(m, W, name, dev, capture, flush, K, W_)
+                for name in ("qwen3_zipf0", "qwen3_zipf0.5", "qwen3_zipf1", "qwen3_zipf1.5",
+                             "qwen3_skew")]
+    else:
+        skew = None
+
     mean_step_ms = max_over_ranks(statistics.mean(step_ms), world)
     sep_step_ms = max_over_ranks(statistics.mean(sep_ms), world)
     e2e_us = max_over_ranks(statistics.mean(e2e_ms), world) * 1000
@@ -565,6 +649,8 @@ def run_ours(args) -> None:
         "separate_calls_us": round(sep_step_ms * 1000, 2),
         "low_latency": ll,
         "signalled": signalled,
+        "send_side_reduction": partial,
+        "routing_skew": skew,
         "dispatch_us": round((favg["route"] + favg["dispatch_fused"]) * 1000, 2),
         "combine_us": round(favg["combine_fused"] * 1000, 2),
         "achieved_gbs": round(achieved, 1),
@@ -614,6 +700,8 @@ def main() -> None:
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="minimum CPU time spent on the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-skew", action="store_true",
+                    help="skip the skewed-routing (Zipf) layer lines")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -113,6 +113,7 @@ int moe_sizes_query(const moe_shape *sh, moe_sizes *out) {
     out->bytes_ll_count = N * E * 4;
     out->bytes_ll_y = out->ll_rows * H * 2;
     out->bytes_sig = (2 * N * N + 4) * 4;
+    out->bytes_part = N * N * T * H * 2;
     return MOE_OK;
 }
 
@@ -233,6 +234,35 @@ int moe_combine_recv(const moe_shape *sh, const uint16_t *csend, const int32_t *
         return MOE_EINVAL;
     return cuda_rc(moe::launch_combine_reduce(*sh, (int)z.cap, csend, topk_idx, topk_w, slot_row,
                                               send_off, csend_off, out_bf16, as_stream(stream)));
+}
+
+int moe_combine_partial_send(const moe_shape *sh, const uint16_t *y_bf16, const int32_t *topk_idx,
+                             const float *topk_w, const int32_t *slot_row,
+                             const int32_t *expert_send_off, const int32_t *seg_off,
+                             uint16_t *part, void *stream) {
+    moe_sizes z;
+    int rc = moe_sizes_query(sh, &z);
+    if (rc != MOE_OK) return rc;
+    if (!ok_ptr(y_bf16, z.bytes_y) || !ok_ptr(topk_idx, z.bytes_topk_idx) ||
+        !ok_ptr(topk_w, z.bytes_topk_idx) || !ok_ptr(slot_row, z.bytes_topk_idx) ||
+        !ok_ptr(expert_send_off, z.bytes_expert_send_off) || !ok_ptr(seg_off, z.bytes_seg_off) ||
+        !ok_ptr(part, z.bytes_part))
+        return MOE_EINVAL;
+    return cuda_rc(moe::launch_combine_partial_send(*sh, (int)z.cap, y_bf16, topk_idx, topk_w,
+                                                    slot_row, expert_send_off, seg_off, part,
+                                                    as_stream(stream)));
+}
+
+int moe_combine_partial_recv(const moe_shape *sh, const uint16_t *part, const int32_t *topk_idx,
+                             const int32_t *slot_row, uint16_t *out_bf16, void *stream) {
+    moe_sizes z;
+    int rc = moe_sizes_query(sh, &z);
+    if (rc != MOE_OK) return rc;
+    if (!ok_ptr(part, z.bytes_part) || !ok_ptr(topk_idx, z.bytes_topk_idx) ||
+        !ok_ptr(slot_row, z.bytes_topk_idx) || !ok_ptr(out_bf16, z.bytes_x))
+        return MOE_EINVAL;
+    return cuda_rc(moe::launch_combine_partial_recv(*sh, part, topk_idx, slot_row, out_bf16,
+                                                    as_stream(stream)));
 }
 
 int moe_expert_standin(const moe_shape *sh, int mode, const uint8_t *grp_q, const float *grp_s,

@@ -1,0 +1,54 @@
+// bf16.cuh -- bf16 <-> fp32 helpers of the combine kernels: round-to-nearest-
+// even packing of two fp32 values, and eight fused multiply-adds of a weight
+// into fp32 accumulators from a 16-byte vector of bf16.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+
+#ifndef MOE_REDUCE_THREADS
+#define MOE_REDUCE_THREADS 64
+#endif
+
+namespace moe {
+
+// 64 threads per token keeps a DeepSeek-V3-sized batch (2048 tokens) within
+// one wave of resident blocks.
+constexpr int kReduceThreads = MOE_REDUCE_THREADS;
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+    const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+    return l | (h << 16);
+}
+
+__device__ __forceinline__ uint4 pack_bf16x8(const float (&a)[8]) {
+    return make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
+                      pack_bf16x2(a[6], a[7]));
+}
+
+__device__ __forceinline__ void fma8(float (&acc)[8], float w, const uint4 &v) {
+    acc[0] = __fmaf_rn(w, bf16_lo(v.x), acc[0]);
+    acc[1] = __fmaf_rn(w, bf16_hi(v.x), acc[1]);
+    acc[2] = __fmaf_rn(w, bf16_lo(v.y), acc[2]);
+    acc[3] = __fmaf_rn(w, bf16_hi(v.y), acc[3]);
+    acc[4] = __fmaf_rn(w, bf16_lo(v.z), acc[4]);
+    acc[5] = __fmaf_rn(w, bf16_hi(v.z), acc[5]);
+    acc[6] = __fmaf_rn(w, bf16_lo(v.w), acc[6]);
+    acc[7] = __fmaf_rn(w, bf16_hi(v.w), acc[7]);
+}
+
+// acc += the eight bf16 values of v (fp32 additions, round to nearest).
+__device__ __forceinline__ void add8(float (&acc)[8], const uint4 &v) {
+    acc[0] = __fadd_rn(acc[0], bf16_lo(v.x));
+    acc[1] = __fadd_rn(acc[1], bf16_hi(v.x));
+    acc[2] = __fadd_rn(acc[2], bf16_lo(v.y));
+    acc[3] = __fadd_rn(acc[3], bf16_hi(v.y));
+    acc[4] = __fadd_rn(acc[4], bf16_lo(v.z));
+    acc[5] = __fadd_rn(acc[5], bf16_hi(v.z));
+    acc[6] = __fadd_rn(acc[6], bf16_lo(v.w));
+    acc[7] = __fadd_rn(acc[7], bf16_hi(v.w));
+}
+
+}  // namespace moe

@@ -6,6 +6,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
+#include "bf16.cuh"
 #include "common.cuh"
 #include "launch.h"
 
@@ -19,30 +20,7 @@ namespace moe {
 // thread takes 16-byte chunks of the row, issues the R loads, and folds them
 // into fp32 accumulators with one fused multiply-add per slot in slot order
 // k = 0..R-1, rounding once to bf16 at the end.
-#ifndef MOE_REDUCE_THREADS
-#define MOE_REDUCE_THREADS 64
-#endif
-// 64 threads per token keeps a DeepSeek-V3-sized batch (2048 tokens) within
-// one wave of resident blocks.
-constexpr int kReduceThreads = MOE_REDUCE_THREADS;
 constexpr int kReduceGroup = 8;  // row loads kept in flight per chunk
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
-    const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
-    return l | (h << 16);
-}
-
-__device__ __forceinline__ void fma8(float (&acc)[8], float w, const uint4 &v) {
-    acc[0] = __fmaf_rn(w, bf16_lo(v.x), acc[0]);
-    acc[1] = __fmaf_rn(w, bf16_hi(v.x), acc[1]);
-    acc[2] = __fmaf_rn(w, bf16_lo(v.y), acc[2]);
-    acc[3] = __fmaf_rn(w, bf16_hi(v.y), acc[3]);
-    acc[4] = __fmaf_rn(w, bf16_lo(v.z), acc[4]);
-    acc[5] = __fmaf_rn(w, bf16_hi(v.z), acc[5]);
-    acc[6] = __fmaf_rn(w, bf16_lo(v.w), acc[6]);
-    acc[7] = __fmaf_rn(w, bf16_hi(v.w), acc[7]);
-}
 
 // kLL: the rows come from the low-latency layout, row ll_row[s][t][k] of
 // `csend` (there y_ll), instead of the combine send buffers.

@@ -71,6 +71,22 @@ cudaError_t launch_combine_fused(const moe_shape &sh, int cap, const uint16_t *y
                                  const int32_t *send_off, const int32_t *csend_off,
                                  uint16_t *csend, uint16_t *out, cudaStream_t st);
 
+// Combine with send-side reduction: partial rows [N][N][T][H] bf16
+// (expert rank, sender, token).
+cudaError_t launch_combine_partial_send(const moe_shape &sh, int cap, const uint16_t *y,
+                                        const int32_t *idx, const float *w,
+                                        const int32_t *slot_row, const int32_t *eso,
+                                        const int32_t *seg_off, uint16_t *pbuf, cudaStream_t st);
+
+cudaError_t launch_combine_partial_recv(const moe_shape &sh, const uint16_t *pbuf,
+                                        const int32_t *idx, const int32_t *slot_row,
+                                        uint16_t *out, cudaStream_t st);
+
+cudaError_t launch_combine_partial(const moe_shape &sh, int cap, const uint16_t *y,
+                                   const int32_t *idx, const float *w, const int32_t *slot_row,
+                                   const int32_t *eso, const int32_t *seg_off, uint16_t *pbuf,
+                                   uint16_t *out, cudaStream_t st);
+
 cudaError_t launch_expert_standin(const moe_shape &sh, int cap, int mode, const uint8_t *grp_q,
                                   const float *grp_s, const int32_t *grp_off, uint16_t *y,
                                   cudaStream_t st);

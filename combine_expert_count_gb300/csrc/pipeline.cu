@@ -15,6 +15,9 @@
 // exchange and then writes its tokens straight to their places ("Send and
 // receive buffers"); with all ranks in one GPU's memory the same knowledge
 // lets the quantiser place each row at its final grouped position.
+// moe_combine_partial: the combine with send-side reduction in one pass --
+//   per token, the partial row of each expert rank is formed from y, written
+//   to its place, and added into the output.
 // moe_dispatch_signalled: k_route, then the send and the receive shuffle as
 //   two groups of CTAs of one co-resident kernel, handing rows over by
 //   per-(sender, receiver) arrival flags.
@@ -107,6 +110,24 @@ extern "C" int moe_combine(const moe_shape *sh, const moe_buffers *b, void *stre
     if (moe::launch_combine_fused(*sh, (int)z.cap, b->y, b->topk_idx, b->topk_w, b->slot_row,
                                   b->expert_send_off, b->seg_off, b->send_off, b->csend_off,
                                   b->csend, b->out, st) != cudaSuccess)
+        return MOE_ECUDA;
+    return MOE_OK;
+}
+
+extern "C" int moe_combine_partial(const moe_shape *sh, const moe_buffers *b, uint16_t *part,
+                                   void *stream) {
+    moe_sizes z;
+    int rc = moe_sizes_query(sh, &z);
+    if (rc != MOE_OK) return rc;
+    if (!b) return MOE_EINVAL;
+    if (!aligned(b->topk_idx, z.bytes_topk_idx) || !aligned(b->topk_w, z.bytes_topk_idx) ||
+        !aligned(b->y, z.bytes_y) || !aligned(b->expert_send_off, z.bytes_expert_send_off) ||
+        !aligned(b->slot_row, z.bytes_topk_idx) || !aligned(b->seg_off, z.bytes_seg_off) ||
+        !aligned(b->out, z.bytes_x) || !aligned(part, z.bytes_part))
+        return MOE_EINVAL;
+    if (moe::launch_combine_partial(*sh, (int)z.cap, b->y, b->topk_idx, b->topk_w, b->slot_row,
+                                    b->expert_send_off, b->seg_off, part, b->out,
+                                    reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return MOE_ECUDA;
     return MOE_OK;
 }

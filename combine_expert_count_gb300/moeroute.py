@@ -35,7 +35,8 @@ MOE_ST_BAD_EXPERT, MOE_ST_CAPACITY, MOE_ST_TIMEOUT = 1, 2, 4
 EXPORTS = ("moe_sizes_query", "moe_route_count", "moe_exchange", "moe_route", "moe_dispatch_send",
            "moe_dispatch_recv", "moe_combine_send", "moe_combine_recv", "moe_dispatch",
            "moe_dispatch_send_recv", "moe_dispatch_signalled", "moe_dispatch_signalled_static",
-           "moe_combine", "moe_expert_standin",
+           "moe_combine", "moe_combine_partial_send", "moe_combine_partial_recv",
+           "moe_combine_partial", "moe_expert_standin",
            "moe_e4m3_encode", "moe_dispatch_ll", "moe_expert_standin_ll", "moe_combine_ll",
            "moe_strerror", "moe_version")
 
@@ -49,7 +50,8 @@ _SIZE_FIELDS = ("cap", "send_rows", "bytes_x", "bytes_topk_idx", "bytes_expert_c
                 "bytes_send_off", "bytes_expert_send_off", "bytes_grp_off", "bytes_seg_off",
                 "bytes_m_sizes", "bytes_send_q", "bytes_send_s", "bytes_send_tok", "bytes_grp_q",
                 "bytes_grp_s", "bytes_grp_src", "bytes_y", "ll_rows", "bytes_ll_q",
-                "bytes_ll_s", "bytes_ll_src", "bytes_ll_count", "bytes_ll_y", "bytes_sig")
+                "bytes_ll_s", "bytes_ll_src", "bytes_ll_count", "bytes_ll_y", "bytes_sig",
+                "bytes_part")
 
 
 class moe_sizes(ctypes.Structure):
@@ -94,6 +96,9 @@ def lib() -> ctypes.CDLL:
             h.moe_dispatch_send_recv.argtypes = [sp, P(moe_buffers), V]
             h.moe_dispatch_signalled.argtypes = [sp, P(moe_buffers), V, V]
             h.moe_dispatch_signalled_static.argtypes = [sp, P(moe_buffers), V]
+            h.moe_combine_partial_send.argtypes = [sp] + [V] * 7 + [V]
+            h.moe_combine_partial_recv.argtypes = [sp] + [V] * 4 + [V]
+            h.moe_combine_partial.argtypes = [sp, P(moe_buffers), V, V]
             h.moe_combine.argtypes = [sp, P(moe_buffers), V]
             h.moe_dispatch_send.argtypes = [sp] + [V] * 6 + [V]
             h.moe_dispatch_recv.argtypes = [sp] + [V] * 10 + [V]
@@ -337,6 +342,41 @@ def moe_combine(shape, tensors: dict, stream=None) -> None:
     _check(lib().moe_combine(ctypes.byref(sh), ctypes.byref(b), _s(stream)), "moe_combine")
 
 
+def moe_combine_partial_send(shape, y, topk_idx, topk_w, slot_row, expert_send_off, seg_off, part,
+                             stream=None) -> None:
+    sh, z = _as_shape(shape), sizes_query(shape)
+    _check(lib().moe_combine_partial_send(
+        ctypes.byref(sh), _p(y, z.bytes_y, "y"), _p(topk_idx, z.bytes_topk_idx, "topk_idx"),
+        _p(topk_w, z.bytes_topk_idx, "topk_w"), _p(slot_row, z.bytes_topk_idx, "slot_row"),
+        _p(expert_send_off, z.bytes_expert_send_off, "expert_send_off"),
+        _p(seg_off, z.bytes_seg_off, "seg_off"), _p(part, z.bytes_part, "part"), _s(stream)),
+        "moe_combine_partial_send")
+
+
+def moe_combine_partial_recv(shape, part, topk_idx, slot_row, out, stream=None) -> None:
+    sh, z = _as_shape(shape), sizes_query(shape)
+    _check(lib().moe_combine_partial_recv(
+        ctypes.byref(sh), _p(part, z.bytes_part, "part"),
+        _p(topk_idx, z.bytes_topk_idx, "topk_idx"), _p(slot_row, z.bytes_topk_idx, "slot_row"),
+        _p(out, z.bytes_x, "out"), _s(stream)),
+        "moe_combine_partial_recv")
+
+
+_PARTIAL_NEEDS = {"topk_idx": "bytes_topk_idx", "topk_w": "bytes_topk_idx", "y": "bytes_y",
+                  "expert_send_off": "bytes_expert_send_off", "slot_row": "bytes_topk_idx",
+                  "seg_off": "bytes_seg_off", "out": "bytes_x"}
+
+
+def moe_combine_partial(shape, tensors: dict, part, stream=None) -> None:
+    """Combine with send-side reduction in one pass; ``part`` receives the
+    partial rows [N][N][T][H] (bf16)."""
+    sh, z = _as_shape(shape), sizes_query(shape)
+    b = _buffers(z, tensors, _PARTIAL_NEEDS)
+    _check(lib().moe_combine_partial(ctypes.byref(sh), ctypes.byref(b),
+                                     _p(part, z.bytes_part, "part"), _s(stream)),
+           "moe_combine_partial")
+
+
 def moe_expert_standin(shape, mode: int, grp_q, grp_s, grp_off, y, stream=None) -> None:
     sh, z = _as_shape(shape), sizes_query(shape)
     _check(lib().moe_expert_standin(
@@ -455,6 +495,14 @@ class MoeBuffers:
         # moe_dispatch_signalled's group counters and flags (zero between calls)
         self.sig = torch.zeros(int(z.bytes_sig) // 4, dtype=torch.int32, device=d)
 
+    def partial_rows(self) -> torch.Tensor:
+        """The send-side reduction's partial rows [N][N][T][H] bf16, allocated
+        on first use."""
+        if not hasattr(self, "part"):
+            N, T, H = self.N, self.T, self.H
+            self.part = torch.empty((N, N, T, H), dtype=torch.bfloat16, device=self.out.device)
+        return self.part
+
     def device_bytes(self) -> int:
         return sum(t.numel() * t.element_size() for t in vars(self).values()
                    if isinstance(t, torch.Tensor))
@@ -520,9 +568,25 @@ class MoeBuffers:
     def combine(self, topk_idx, topk_w, y=None, out=None, stream=None,
                 calls: str = "fused") -> torch.Tensor:
         """The combine half; returns ``out``.  ``calls``: "fused" (one
-        moe_combine call) or anything else for moe_combine_send then
+        moe_combine call), "partial" (one moe_combine_partial call: send-side
+        reduction), "partial_separate" (moe_combine_partial_send then
+        moe_combine_partial_recv) or anything else for moe_combine_send then
         moe_combine_recv."""
         out = self.out if out is None else out
+        if calls in ("partial", "partial_separate"):
+            part = self.partial_rows()
+            if calls == "partial":
+                b = self._struct(_PARTIAL_NEEDS, topk_idx=topk_idx, topk_w=topk_w,
+                                 y=self.y if y is None else y, out=out)
+                _check(lib().moe_combine_partial(ctypes.byref(self.shape), ctypes.byref(b),
+                                                 ctypes.c_void_p(part.data_ptr()), _s(stream)),
+                       "moe_combine_partial")
+            else:
+                moe_combine_partial_send(self.shape, self.y if y is None else y, topk_idx, topk_w,
+                                         self.slot_row, self.expert_send_off, self.seg_off, part,
+                                         stream)
+                moe_combine_partial_recv(self.shape, part, topk_idx, self.slot_row, out, stream)
+            return out
         if calls == "fused":
             b = self._struct(_COMBINE_NEEDS, topk_idx=topk_idx, topk_w=topk_w,
                              y=self.y if y is None else y, out=out)

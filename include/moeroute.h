@@ -133,6 +133,7 @@ typedef struct {
     int64_t bytes_ll_count; /* N*E*4: [N][Er][N] */
     int64_t bytes_ll_y;     /* ll_rows * H * 2 (bf16 expert outputs) */
     int64_t bytes_sig;      /* (2*N*N + 4) * 4: moe_dispatch_signalled's flags */
+    int64_t bytes_part;     /* N*N*T*H * 2: send-side-reduction partial rows */
 } moe_sizes;
 
 /* Fill *out for *shape.  Host only.  MOE_EINVAL / MOE_ENOTSUP on a bad shape. */
@@ -293,6 +294,44 @@ int moe_dispatch(const moe_shape *shape, const moe_buffers *b, void *stream);
  * topk_w, the routing arrays (from a dispatch of the same topk_idx), csend
  * and out.  Outputs: csend and out, as the two separate calls write them. */
 int moe_combine(const moe_shape *shape, const moe_buffers *b, void *stream);
+
+/* ---------------------------------------------------------------- send-side reduction
+ * The combine with send-side accumulation, the alternative the EFA page's
+ * evaluation ("Evaluation: dispatch/combine latency", prefill) contrasts with
+ * its receive-side-only accumulation: summing on the sending side cuts the
+ * bytes sent, with some risk to accuracy.  On expert rank r, for each token t
+ * of each rank s with at least one expert on r, the weighted outputs of those
+ * experts are summed (fp32 fused multiply-add in slot order; an output whose
+ * grouped row was dropped at capacity counts as zero) and rounded once to
+ * bf16:
+ *   part     bf16  [N][N][T][H]   row (r, s, t); rows of an (r, s, t) without
+ *                                 an expert of r are left untouched
+ * The receiver adds its token's partial rows in ascending rank order in fp32
+ * and rounds once to bf16 (0 for a token without valid experts).  Against
+ * the exact weighted sum X: |out - X| <= 2^-7 * sum_k |w_k y_k| (one bf16
+ * rounding per partial and one at the end) -- a different result from
+ * moe_combine_recv, whose one rounding gives |out - X| <= 2^-8 |X| + fp32
+ * error.  Bytes sent: one row per (token, expert rank) instead of one per
+ * (token, expert).  Host errors as above; no status bits. */
+
+/* Sending side: writes the partial rows.  y, topk_idx, topk_w, slot_row,
+ * expert_send_off, seg_off as for moe_combine_send / moe_combine_recv. */
+int moe_combine_partial_send(const moe_shape *shape, const uint16_t *y_bf16,
+                             const int32_t *topk_idx, const float *topk_w,
+                             const int32_t *slot_row, const int32_t *expert_send_off,
+                             const int32_t *seg_off, uint16_t *part, void *stream);
+
+/* Receiving side: out[s][t] = bf16_rn(sum over ranks r of the token's experts,
+ * ascending, of part[r][s][t]).  out may be pinned host memory. */
+int moe_combine_partial_recv(const moe_shape *shape, const uint16_t *part,
+                             const int32_t *topk_idx, const int32_t *slot_row,
+                             uint16_t *out_bf16, void *stream);
+
+/* Both in one pass: each partial row is formed once, written to part and
+ * added into out.  Uses y, topk_idx, topk_w, slot_row, expert_send_off,
+ * seg_off and out of *b. */
+int moe_combine_partial(const moe_shape *shape, const moe_buffers *b, uint16_t *part,
+                        void *stream);
 
 /* ---------------------------------------------------------------- signalled
  * moe_route, then the dispatch send and the dispatch receive shuffle in ONE

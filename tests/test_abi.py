@@ -71,6 +71,7 @@ def test_sizes_query_matches_layout(lib, name):
     assert z.ll_rows == N * E * T and z.bytes_ll_q == N * E * T * H
     assert z.bytes_ll_count == N * E * 4 and z.bytes_ll_y == N * E * T * H * 2
     assert z.bytes_sig == (2 * N * N + 4) * 4
+    assert z.bytes_part == N * N * T * H * 2
     z2 = m.sizes_query(m.make_shape(w.N, w.T, w.E, w.R, w.H, 100))
     assert z2.cap == 100 and z2.bytes_grp_q == N * 100 * H
 
@@ -103,7 +104,8 @@ def test_null_and_misaligned_pointers_rejected(lib):
     calls = {
         "moe_route_count": 6, "moe_exchange": 7, "moe_route": 10, "moe_dispatch_send": 6,
         "moe_dispatch_recv": 10, "moe_combine_send": 8, "moe_combine_recv": 8,
-        "moe_dispatch_ll": 8, "moe_combine_ll": 5,
+        "moe_dispatch_ll": 8, "moe_combine_ll": 5, "moe_combine_partial_send": 7,
+        "moe_combine_partial_recv": 4,
     }
     for name, nptr in calls.items():
         fn = getattr(L, name)
@@ -120,6 +122,14 @@ def test_null_and_misaligned_pointers_rejected(lib):
             setattr(b, field, 0x10004)
             assert fn(ctypes.byref(sh), ctypes.byref(b), None) == m.MOE_EINVAL, field
     full = m.moe_buffers(*([0x10000] * len(m._BUFFER_FIELDS)))
+    for part in (bad, null):
+        assert L.moe_combine_partial(ctypes.byref(sh), ctypes.byref(full), part,
+                                     None) == m.MOE_EINVAL
+    for field in list(m._PARTIAL_NEEDS):
+        b = m.moe_buffers(*([0x10000] * len(m._BUFFER_FIELDS)))
+        setattr(b, field, 0x10004)
+        assert L.moe_combine_partial(ctypes.byref(sh), ctypes.byref(b), good,
+                                     None) == m.MOE_EINVAL, field
     for sig in (bad, null):
         assert L.moe_dispatch_signalled(ctypes.byref(sh), ctypes.byref(full), sig,
                                         None) == m.MOE_EINVAL
