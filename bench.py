@@ -684,6 +684,40 @@ def run_ours(args) -> None:
     print(json.dumps(line), flush=True)
 
 
+def profile_pass(args) -> None:
+    """A fixed launch sequence for a profiler, nothing timed: every kernel of
+    the main path, the separate calls, the signalled dispatch and the
+    send-side-reduction combine, twice (the first pass warms up).  The
+    low-latency layout is left out (its fixed regions hold several GB)."""
+    import torch
+
+    from combine_expert_count_gb300 import moeroute as m
+    from combine_expert_count_gb300 import workloads as W
+
+    w = W.CONFIGS[args.config]
+    d = W.generate(w)
+    buf = m.MoeBuffers(w.N, w.T, w.E, w.R, w.H, cap=args.cap)
+    x = torch.from_numpy(d["x"].view(np.int16)).cuda()
+    idx = torch.from_numpy(d["topk_idx"]).cuda()
+    wt = torch.from_numpy(d["topk_w"]).cuda()
+    mode = 1 if w.expert == "scale" else 0
+    buf.dispatch(x, idx)
+    buf.expert(mode)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        buf.dispatch(x, idx)                          # k_route_cluster, dispatch fused
+        buf.combine(idx, wt)                          # k_combine_fused
+        buf.dispatch(x, idx, calls="fused_route")     # route, quant + pack, receive shuffle
+        buf.combine(idx, wt, calls="separate")        # combine pack, combine reduce
+        buf.dispatch(x, idx, calls="signalled")       # route, signalled dispatch
+        buf.combine(idx, wt, calls="partial")         # send-side reduction, one pass
+        buf.combine(idx, wt, calls="partial_separate")
+        torch.cuda.synchronize()
+    if int(buf.status.item()) != 0:
+        raise RuntimeError(f"device status {int(buf.status.item())}")
+    print("profile pass done: 13 library launches per pass", flush=True)
+
+
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -702,8 +736,12 @@ def main() -> None:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-skew", action="store_true",
                     help="skip the skewed-routing (Zipf) layer lines")
+    ap.add_argument("--profile-pass", action="store_true",
+                    help="run every kernel twice without timing (for ncu) and exit")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.profile_pass:
+        profile_pass(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
