@@ -96,11 +96,13 @@ def measured_peak():
 KERNEL_SOURCES = {
     "route": ("route.cu", "common.cuh"),
     "dispatch_fused": ("dispatch.cu", "shuffle.cuh", "common.cuh"),
-    "combine_fused": ("combine.cu", "common.cuh"),
+    "combine_fused": ("combine.cu", "bf16.cuh", "common.cuh"),
     "dispatch_send": ("dispatch.cu", "shuffle.cuh", "common.cuh"),
     "dispatch_recv": ("shuffle.cu", "shuffle.cuh", "common.cuh"),
     "combine_send": ("shuffle.cu", "shuffle.cuh", "common.cuh"),
-    "combine_recv": ("combine.cu", "common.cuh"),
+    "combine_recv": ("combine.cu", "bf16.cuh", "common.cuh"),
+    "combine_partial": ("partial.cu", "bf16.cuh", "common.cuh"),
+    "dispatch_signalled": ("dispatch.cu", "shuffle.cuh", "common.cuh"),
 }
 
 
