@@ -3,6 +3,13 @@
 // instead of a caller-supplied buffer, so the call allocates nothing and
 // asks the caller for nothing beyond moe_dispatch's buffers.
 //
+// It is for callers that cannot allocate device memory at the point where
+// they dispatch: a serving process that splits the GPU's memory into its
+// own arenas at start-up and must not call cudaMalloc while it serves (the
+// call could fail under memory pressure or break the plan), or a C program
+// that receives the moe_buffers set from another framework's allocator and
+// has no allocator of its own for the extra flag buffer.
+//
 // The array holds the scratch of shapes up to MOE_SIG_STATIC_MAX_N ranks:
 // 2*N*N group counters and flags plus a completion counter, 32,784 bytes.
 // Its address is looked up once per device (cudaGetSymbolAddress with that

@@ -1,8 +1,13 @@
-"""moe_dispatch_signalled_static (the signalled dispatch with the library's
-own static flag scratch, no allocation) against moe_dispatch_signalled with
-a caller scratch, through the C ABI, over two calls in a row with different
-inputs.  This file is collected last so that it also runs after every other
-GPU test in the same process."""
+"""moe_dispatch_signalled_static against moe_dispatch_signalled, through the
+C ABI, over two calls in a row with different inputs.
+
+The static entry keeps the signalled dispatch's flag scratch in a device
+array of the library, for callers that cannot allocate that buffer: a
+serving process that fixes its device-memory plan at start-up and must not
+allocate while serving, or a C caller that only holds the buffers another
+framework allocated.  Its outputs must equal the caller-scratch entry's bit
+for bit.  This file is collected last, so a run that stops at the first
+failure has already run every other test; it also passes on its own."""
 from __future__ import annotations
 
 import numpy as np
