@@ -1,9 +1,10 @@
 // common.cuh -- device helpers shared by the libmoeroute kernels (sm_103a).
 //
 // Warp / block scans, the status word, and thin inline-PTX wrappers for the
-// mbarrier and bulk-async-copy (TMA, non-tensor) instructions the row
-// shuffles use.  Every wait on an mbarrier is bounded by a cycle budget and
-// reports MOE_ST_TIMEOUT instead of spinning forever.
+// mbarrier and bulk-async-copy (TMA, non-tensor) loads the quantiser uses and
+// the acquire / release flag accesses of the signalled dispatch.  Every wait
+// on an mbarrier is bounded by a cycle budget and reports MOE_ST_TIMEOUT
+// instead of spinning forever.
 #pragma once
 
 #include <cstdint>
@@ -100,46 +101,6 @@ __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src, uint32
             smem_addr(dst_smem)),
         "l"(src), "r"(bytes), "r"(smem_addr(bar))
         : "memory");
-}
-
-// Bulk copy shared -> global, tracked by bulk groups.
-__device__ __forceinline__ void bulk_s2g(void *dst, const void *src_smem, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
-                 "r"(smem_addr(src_smem)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() {
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-// Wait until at most N committed bulk groups still have to read shared memory.
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-// Order this thread's generic-proxy writes to shared memory before later
-// async-proxy (bulk copy) reads of it.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// Wait until every committed bulk group has completed (writes performed).
-__device__ __forceinline__ void bulk_wait_all() {
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
-// Wait until at most N committed bulk groups are still incomplete.
-template <int N>
-__device__ __forceinline__ void bulk_wait() {
-    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// Order this thread's completed async-proxy (bulk copy) writes to global
-// memory before its later generic-proxy operations (a release, a flag).
-__device__ __forceinline__ void fence_proxy_async_global() {
-    asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // GPU-scope acquire load / release store of a 32-bit flag.

@@ -344,8 +344,8 @@ int moe_combine_partial(const moe_shape *shape, const moe_buffers *b, uint16_t *
  * send rows exactly as moe_dispatch_send; each (sender s, receiver r) group
  * is the run of s's send buffer bound for r (send_off[s][r] ..
  * send_off[s][r+1]).  Every row written adds one to the group's counter
- * after its store has completed and a release fence; the writer that
- * completes the group sets its flag.  Receiving CTAs copy each send row to
+ * after a CTA barrier and a release fence that order the row's stores
+ * before it; the writer that completes the group sets its flag.  Receiving CTAs copy each send row to
  * its grouped row exactly as moe_dispatch_recv, once the row's group flag is
  * set, so a receiver starts on sender s while later senders are still being
  * packed.  Outputs: everything moe_dispatch writes, bit for bit.
