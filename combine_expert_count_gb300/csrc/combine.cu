@@ -22,6 +22,17 @@ namespace moe {
 // k = 0..R-1, rounding once to bf16 at the end.
 constexpr int kReduceGroup = 8;  // row loads kept in flight per chunk
 
+// Store of one 16-byte vector of a row written once and not read back here.
+#ifndef MOE_STREAM_STORES
+#define MOE_STREAM_STORES 0
+#endif
+__device__ __forceinline__ void st_row(uint4 *p, const uint4 &v) {
+    if (MOE_STREAM_STORES)
+        __stcs(p, v);
+    else
+        *p = v;
+}
+
 // kLL: the rows come from the low-latency layout, row ll_row[s][t][k] of
 // `csend` (there y_ll), instead of the combine send buffers.
 template <bool kLL>
@@ -118,7 +129,7 @@ cudaError_t launch_combine_ll(const moe_shape &sh, const uint16_t *y_ll, const f
 // moe_combine_recv would after reading them back.  A row whose grouped
 // position was dropped is written as zeros and contributes w * 0.
 template <int KR>  // 0: slots read from shared memory; else R <= KR slots held in registers
-__global__ void __launch_bounds__(kReduceThreads)
+__global__ void __launch_bounds__(kGatherThreads)
     k_combine_fused(int N, int T, int E, int R, int H, int cap, const uint16_t *__restrict__ y,
                     const int32_t *__restrict__ idx, const float *__restrict__ w,
                     const int32_t *__restrict__ slot_row, const int32_t *__restrict__ eso,
@@ -173,7 +184,7 @@ __global__ void __launch_bounds__(kReduceThreads)
 #pragma unroll
                 for (int u = 0; u < KR; ++u) {
                     if (cs[u]) {
-                        cs[u][part] = v[u];
+                        st_row(cs[u] + part, v[u]);
                         fma8(acc, wr[u], v[u]);
                     }
                 }
@@ -226,7 +237,7 @@ cudaError_t launch_combine_fused(const moe_shape &sh, int cap, const uint16_t *y
     if (ntok <= 0) return cudaSuccess;
     const int grid = (int)(ntok < (1LL << 30) ? ntok : (1LL << 30));
     auto kern = sh.R <= 8 ? k_combine_fused<8> : k_combine_fused<0>;
-    return launch_kernel(kern, dim3((unsigned)grid), dim3(kReduceThreads), 0, st, sh.N, sh.T, sh.E,
+    return launch_kernel(kern, dim3((unsigned)grid), dim3(kGatherThreads), 0, st, sh.N, sh.T, sh.E,
                          sh.R, sh.H, cap, y, idx, w, slot_row, eso, seg_off, send_off, csend_off,
                          csend, out);
 }

@@ -20,12 +20,13 @@
 
 namespace moe {
 
-static_assert(kReduceThreads >= 32, "warp 0 sorts the slots");
+static_assert(kReduceThreads >= 32 && kGatherThreads >= 32, "warp 0 sorts the slots");
 
 enum class PartialMode { kSend, kRecv, kFused };
 
 template <PartialMode kMode, int KR>  // KR > 0: R <= KR rows in registers; 0: any R
-__global__ void __launch_bounds__(kReduceThreads)
+__global__ void __launch_bounds__(kGatherThreads > kReduceThreads ? kGatherThreads
+                                                                   : kReduceThreads)
     k_combine_partial(int N, int T, int E, int R, int H, int cap, const uint16_t *__restrict__ y,
                       const int32_t *__restrict__ idx, const float *__restrict__ w,
                       const int32_t *__restrict__ slot_row, const int32_t *__restrict__ eso,
@@ -165,7 +166,9 @@ static cudaError_t launch_partial(const moe_shape &sh, int cap, const uint16_t *
     if (ntok <= 0) return cudaSuccess;
     const int grid = (int)(ntok < (1LL << 30) ? ntok : (1LL << 30));
     auto kern = sh.R <= 8 ? k_combine_partial<kMode, 8> : k_combine_partial<kMode, 0>;
-    return launch_kernel(kern, dim3((unsigned)grid), dim3(kReduceThreads), 0, st, sh.N, sh.T,
+    // the receiving side only reads rows: the smaller block (see bf16.cuh)
+    const int threads = kMode == PartialMode::kRecv ? kReduceThreads : kGatherThreads;
+    return launch_kernel(kern, dim3((unsigned)grid), dim3(threads), 0, st, sh.N, sh.T,
                          sh.E, sh.R, sh.H, cap, y, idx, w, slot_row, eso, seg_off, pbuf, out);
 }
 
