@@ -23,6 +23,8 @@ constexpr int kRouteThreads = 1024;
 static size_t route_smem(int E) { return (size_t)E * 3 * sizeof(int) + (size_t)E * 32 * 4; }
 
 // Sender role of rank s = blockIdx.x: counts, scans and stable slots.
+// Returns (the same in every thread) whether an id was outside [0, E); the
+// caller raises MOE_ST_BAD_EXPERT.
 //
 // Stable slots, one chunk of blockDim.x assignments at a time: a lane's rank
 // among equal experts in its warp comes from __match_any_sync; the count of
@@ -30,13 +32,13 @@ static size_t route_smem(int E) { return (size_t)E * 3 * sizeof(int) + (size_t)E
 // table in which each warp's leader stores (chunk stamp << 16 | count);
 // entries with another chunk's stamp read as zero, so the table is never
 // cleared.  run[e] carries earlier chunks.
-__device__ __forceinline__ void route_sender(int N, int T, int E, int R,
+__device__ __forceinline__ bool route_sender(int N, int T, int E, int R,
                                              const int32_t *__restrict__ idx,
                                              int32_t *__restrict__ cnt_out,
                                              int32_t *__restrict__ send_off,
                                              int32_t *__restrict__ eso_out,
                                              int32_t *__restrict__ slot_row,
-                                             int32_t *__restrict__ status, int *smem) {
+                                             int *smem) {
     int *cnt = smem;      // [E] counts
     int *base = cnt + E;  // [E] exclusive scan of counts
     int *run = base + E;  // [E] assignments seen in earlier chunks
@@ -66,7 +68,7 @@ __device__ __forceinline__ void route_sender(int N, int T, int E, int R,
         else
             bad = 1;
     }
-    if (__syncthreads_or(bad) && tid == 0) flag(status, MOE_ST_BAD_EXPERT);
+    const bool any_bad = __syncthreads_or(bad) != 0;
 
     // 2. exclusive scan over experts (E <= blockDim.x: one expert per thread)
     int v = tid < E ? cnt[tid] : 0;
@@ -122,6 +124,7 @@ __device__ __forceinline__ void route_sender(int N, int T, int E, int R,
             __syncthreads();
         }
     }
+    return any_bad;
 }
 
 __global__ void __launch_bounds__(kRouteThreads, 1)
@@ -130,7 +133,9 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
                   int32_t *__restrict__ eso_out, int32_t *__restrict__ slot_row,
                   int32_t *__restrict__ status) {
     extern __shared__ int smem[];
-    route_sender(N, T, E, R, idx, cnt_out, send_off, eso_out, slot_row, status, smem);
+    if (route_sender(N, T, E, R, idx, cnt_out, send_off, eso_out, slot_row, smem) &&
+        threadIdx.x == 0)
+        flag(status, MOE_ST_BAD_EXPERT);
 }
 
 // Receiver role of rank r = blockIdx.x given v = the count of run f = j*N + s
@@ -236,7 +241,9 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     if (tid < N)
         for (int j = 0; j < Er; ++j) w += rc[tid * Er + j];
     route_receiver(N, E, cap, v, w, grp_off, seg_off, csend_off, m_sizes, status);
-    route_sender(N, T, E, R, idx, cnt_out, send_off, eso_out, slot_row, status, smem);
+    if (route_sender(N, T, E, R, idx, cnt_out, send_off, eso_out, slot_row, smem) &&
+        threadIdx.x == 0)
+        flag(status, MOE_ST_BAD_EXPERT);
 }
 
 cudaError_t launch_route_count(const moe_shape &sh, const int32_t *idx, int32_t *cnt,
@@ -266,7 +273,8 @@ cudaError_t launch_route_count(const moe_shape &sh, const int32_t *idx, int32_t 
 // blocks meet at a cluster barrier (release / acquire at cluster scope), and
 // each block then plays receiver, reading the other senders' counts back
 // through L2 -- the routing-information exchange of the pages, between the
-// SMs of one cluster.
+// SMs of one cluster.  Block 0 clears *status before the barrier and every
+// status bit is raised after it, so no separate clear precedes the launch.
 __global__ void __launch_bounds__(kRouteThreads, 1)
     k_route_cluster(int N, int T, int E, int R, int cap, const int32_t *__restrict__ idx,
                     int32_t *__restrict__ cnt_out, int32_t *__restrict__ send_off,
@@ -275,10 +283,12 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
                     int32_t *__restrict__ csend_off, int32_t *__restrict__ m_sizes,
                     int32_t *__restrict__ status) {
     extern __shared__ int smem[];
-    route_sender(N, T, E, R, idx, cnt_out, send_off, eso_out, slot_row, status, smem);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *status = 0;
+    const bool bad = route_sender(N, T, E, R, idx, cnt_out, send_off, eso_out, slot_row, smem);
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
     const int r = blockIdx.x, tid = threadIdx.x, Er = E / N, F = Er * N;
+    if (bad && tid == 0) flag(status, MOE_ST_BAD_EXPERT);
     const int j = tid / N, s = tid - (tid / N) * N;
     // written by other blocks in this launch: read through L2, not the read-only path
     const int v = tid < F ? __ldcg(cnt_out + (size_t)s * E + r * Er + j) : 0;
@@ -329,11 +339,9 @@ cudaError_t launch_route(const moe_shape &sh, int cap, const int32_t *idx, int32
                          int32_t *send_off, int32_t *eso, int32_t *slot_row, int32_t *grp_off,
                          int32_t *seg_off, int32_t *csend_off, int32_t *m_sizes, int32_t *status,
                          cudaStream_t st) {
-    cudaError_t err = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
-    if (err != cudaSuccess) return err;
     static int attr_dev = -1;
     int dev = 0;
-    err = cudaGetDevice(&dev);
+    cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev != attr_dev) {
         err = cudaFuncSetAttribute(k_route, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -354,10 +362,13 @@ cudaError_t launch_route(const moe_shape &sh, int cap, const int32_t *idx, int32
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
+        // the kernel clears *status itself
         return cudaLaunchKernelEx(&cfg, k_route_cluster, sh.N, sh.T, sh.E, sh.R, cap, idx, cnt,
                                   send_off, eso, slot_row, grp_off, seg_off, csend_off, m_sizes,
                                   status);
     }
+    err = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
+    if (err != cudaSuccess) return err;
     k_route<<<sh.N, kRouteThreads, route_smem(sh.E), st>>>(sh.N, sh.T, sh.E, sh.R, cap, idx, cnt,
                                                          send_off, eso, slot_row, grp_off, seg_off,
                                                          csend_off, m_sizes, status);
