@@ -158,7 +158,7 @@ __device__ __forceinline__ void quant_pack_body(
     __shared__ uint64_t xbar[2];
     __shared__ long long rows[MOE_MAX_TOPK];   // destination rows of the current item
     __shared__ long long grows[MOE_MAX_TOPK];  // and its grouped rows (kGrouped)
-    __shared__ int ek[MOE_MAX_TOPK], uk[MOE_MAX_TOPK];
+    __shared__ int wpart[8][MOE_MAX_TOPK];  // LL: per-warp counts of earlier equal ids
     int *hist = reinterpret_cast<int *>(sm + stage_bytes(P));  // [E], LL
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthr = blockDim.x;
@@ -200,18 +200,28 @@ __device__ __forceinline__ void quant_pack_body(
         if (!kHostX && tid == 0 && item + G < nitems) issue_load(item + G, b ^ 1);
         if constexpr (kLL) {
             // rows of this token in the low-latency layout, while x arrives:
-            // u_k = earlier assignments of rank s with the same expert
+            // u_k = earlier assignments of rank s with the same expert, eight
+            // slots at a time, counted in registers and summed per warp
             const int32_t *ids = ll.idx + s * TR;
-            if (tid < R) {
-                ek[tid] = __ldg(ll.idx + tok * R + tid);
-                uk[tid] = 0;
-            }
-            __syncthreads();
-            const int lim = t * R + R - 1;
-            for (int i = tid; i < lim; i += nthr) {
-                const int v = __ldg(ids + i);
-                for (int k = 0; k < R; ++k)
-                    if (v == ek[k] && i < t * R + k) atomicAdd(&uk[k], 1);
+            const int lim = t * R + R - 1;  // flat indices before the last slot
+            for (int k0 = 0; k0 < R; k0 += 8) {
+                int ekr[8], c[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    ekr[u] = k0 + u < R ? __ldg(ll.idx + tok * R + k0 + u) : 0;
+                    c[u] = 0;
+                }
+                for (int i = tid; i < lim; i += nthr) {
+                    const int v = __ldg(ids + i);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        c[u] += (k0 + u < R && v == ekr[u] && i < t * R + k0 + u) ? 1 : 0;
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int tot = (int)__reduce_add_sync(kFull, (unsigned)c[u]);
+                    if (lane == 0 && k0 + u < R) wpart[warp][k0 + u] = tot;
+                }
             }
             if (t == 0 && piece == 0) {  // region counts of rank s, once
                 for (int e = tid; e < ll.E; e += nthr) hist[e] = 0;
@@ -234,7 +244,9 @@ __device__ __forceinline__ void quant_pack_body(
             }
             __syncthreads();
             if (tid < R) {
-                const int e = ek[tid], u = uk[tid];
+                const int e = __ldg(ll.idx + tok * R + tid);
+                int u = 0;
+                for (int w = 0; w < (nthr >> 5); ++w) u += wpart[w][tid];
                 const long long row =
                     ((unsigned)e < (unsigned)ll.E && u < T) ? ((long long)e * ll.N + s) * T + u : -1;
                 prow = row;
