@@ -43,11 +43,12 @@ FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 512 << 20
 KERNELS = ("route", "dispatch_send", "dispatch_recv", "combine_send", "combine_recv")
 FUSED = ("route", "dispatch_fused", "combine_fused")
-KERNEL_SYMBOL = {"route": "k_route (route_count + exchange)",
-                 "dispatch_send": "k_quant_pack_staged<false>",
+KERNEL_SYMBOL = {"route": "k_route_cluster (route_count + exchange)",
+                 "dispatch_send": "k_quant_pack_staged<kSend>",
                  "dispatch_recv": "k_row_copy<DispatchMap>",
                  "combine_send": "k_row_copy<CombineMap>", "combine_recv": "k_combine_reduce",
-                 "dispatch_fused": "k_quant_pack_staged<true> (quantise + pack + receive shuffle)",
+                 "dispatch_fused": "k_quant_pack_staged<kSendGrouped> (quantise + pack + receive "
+                                   "shuffle)",
                  "combine_fused": "k_combine_fused (combine send + receive)"}
 
 
