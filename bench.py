@@ -301,6 +301,152 @@ def run_reference(args) -> None:
     print(json.dumps(line), flush=True)
 
 
+def per_kernel_table(nbytes, favg, savg, rcx_k, A, w, workload) -> list:
+    """Each kernel: event time (eager, L2 flushed), algorithmic bytes and GB/s,
+    and where a committed ncu capture of the same source exists, its DRAM
+    bytes per launch, GB/s and the ratio DRAM / algorithmic.  The routing
+    kernels are latency-bound (a few KB): no roofline."""
+    ids = 4 * w.N * w.T * w.R
+    rows = []
+    table = [("route_count", statistics.mean(rcx_k[0]), 2 * ids + 4 * w.N * w.E, None),
+             ("exchange", statistics.mean(rcx_k[1]), 8 * w.N * w.E, None),
+             ("route", favg["route"], nbytes["fused"]["route"], "route")]
+    for k in ("dispatch_send", "dispatch_recv", "combine_send", "combine_recv"):
+        table.append((k, savg[k], nbytes["separate"][k], k))
+    for k in ("dispatch_fused", "combine_fused"):
+        table.append((k, favg[k], nbytes["fused"][k], k))
+    for name, ms, alg, key in table:
+        r = {"kernel": name, "us": round(ms * 1000, 2), "algorithmic_mb": round(alg / 1e6, 2)}
+        if name in ("route_count", "exchange", "route"):
+            r["bound"] = "latency"
+        else:
+            r["algorithmic_gbs"] = round(alg / (ms * 1e-3) / 1e9, 1)
+            dram = dram_traffic(key, workload) if key else None
+            if dram is not None:
+                r["dram_mb"] = round(dram / 1e6, 1)
+                r["dram_gbs"] = round(dram / (ms * 1e-3) / 1e9, 1)
+                r["dram_over_algorithmic"] = round(dram / alg, 3)
+        rows.append(r)
+    return rows
+
+
+def config_line(m, W, name, dev, capture, flush, K, W_) -> dict:
+    """Fused and separate-call layer times on another configuration, against
+    the 70%-of-nominal target of the separate calls' algorithmic bytes."""
+    import torch
+    w = W.CONFIGS[name]
+    d = W.generate(w)
+    b = m.MoeBuffers(w.N, w.T, w.E, w.R, w.H, device=dev)
+    x = torch.from_numpy(d["x"].view(np.int16)).to(dev)
+    idx = torch.from_numpy(d["topk_idx"]).to(dev)
+    wt = torch.from_numpy(d["topk_w"]).to(dev)
+    b.dispatch(x, idx)
+    b.expert(1 if w.expert == "scale" else 0)
+    b.combine(idx, wt)
+    torch.cuda.synchronize()
+    if int(b.status.item()) != 0:
+        raise RuntimeError(f"{name}: device status {int(b.status.item())}")
+    A = int(b.send_off[:, -1].sum().item())
+    nb = algorithmic_bytes(w, A)
+    st = torch.cuda.current_stream()
+    res = {"workload": f"{name}: N={w.N} T={w.T} H={w.H} E={w.E} top-{w.R}, cap={b.cap}"}
+    for key, calls in (("us", "fused"), ("separate_calls_us", "separate")):
+        once = capture(lambda: (b.dispatch(x, idx, calls=calls), b.combine(idx, wt, calls=calls)))
+        for _ in range(W_):
+            flush.zero_()
+            once()
+        tt = []
+        for _ in range(K):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            once()
+            e1.record(st)
+            tt.append((e0, e1))
+        torch.cuda.synchronize()
+        res[key] = round(statistics.mean(a.elapsed_time(c) for a, c in tt) * 1000, 2)
+    moved = sum(nb["fused"].values())
+    s8d = nb["s8d_dispatch"] + nb["s8d_combine"]
+    res["achieved_gbs"] = round(moved / (res["us"] * 1e-6) / 1e9, 1)
+    res["algorithmic_mb_s8d"] = round(s8d / 1e6, 1)
+    res["target_us_70pct_nominal"] = round(s8d / (0.7 * NOMINAL_HBM_GBS * 1e9) * 1e6, 1)
+    del b
+    torch.cuda.empty_cache()
+    return res
+
+
+def oracle_table(args) -> None:
+    """The CPU oracle, as it stands, per configuration and phase (dispatch =
+    route_count + exchange + dispatch_send + dispatch_recv; combine =
+    combine_send + combine_recv), single-threaded on a token sample scaled to
+    the full layer, and the whole layer on all host cores (one process per
+    core, each on its own sample); one JSON line."""
+    import multiprocessing as mp
+    import platform
+    from combine_expert_count_gb300 import workloads as W
+    from oracle import ref
+    ref.build()
+    out = {"cpu": platform.processor() or platform.machine(), "nproc": os.cpu_count(),
+           "configs": []}
+    for name in ("tiny", "dsv3_decode", "kimi_k2_decode", "qwen3_skew", "prefill"):
+        w = W.CONFIGS[name]
+        sample_T = min(w.T, 16 if w.T >= 16 else w.T)
+        ws = w.replace(T=sample_T, seed=w.seed + 17)
+        d = W.generate(ws)
+        t = oracle_phases(ws, d)
+        scale = w.T / sample_T
+        out["configs"].append({"workload": name, "sample_tokens_per_rank": sample_T,
+                               "dispatch_us": round(t[0] * scale * 1e6, 1),
+                               "combine_us": round(t[1] * scale * 1e6, 1)})
+    # all cores: one process per core, each timing a layer sample of dsv3_decode
+    n = os.cpu_count() or 1
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(n) as pool:
+        pool.map(_oracle_worker, [0] * n)  # start-up and build, untimed
+        t0 = time.perf_counter()
+        per = pool.map(_oracle_worker, [1] * n)
+        wall = time.perf_counter() - t0
+    w = W.CONFIGS["dsv3_decode"]
+    out["all_cores_dsv3_decode"] = {
+        "processes": n, "layers": n, "wall_s": round(wall, 3),
+        "us_per_layer": round(wall / n * (w.T / 16) * 1e6, 1),
+        "single_process_s_per_sample": round(statistics.median(per), 3),
+        "how": "n processes, each one 16-token-per-rank layer sample; wall / n, scaled x8"}
+    print(json.dumps(out), flush=True)
+
+
+def oracle_phases(ws, d):
+    from oracle import ref
+    mode = 1 if ws.expert == "scale" else 0
+    t0 = time.perf_counter()
+    rc = ref.route_count(ws.N, ws.T, ws.E, ws.R, d["topk_idx"])
+    ex = ref.exchange(ws.N, ws.E, 1 << 30, rc["expert_count"], rc["send_off"])
+    cap = max(1, int(ex["grp_off"][:, -1].max()))  # exact fit: the oracle's buffers stay small
+    ds = ref.dispatch_send(ws.N, ws.T, ws.R, ws.H, d["x"], rc["slot_row"])
+    dr = ref.dispatch_recv(ws.N, ws.T, ws.E, ws.R, ws.H, cap, ds["send_q"], ds["send_s"],
+                           ds["send_tok"], rc["expert_count"], rc["expert_send_off"], ex["seg_off"])
+    t1 = time.perf_counter()
+    y = ref.expert_standin(ws.N, ws.E, ws.H, cap, mode, dr["grp_q"], dr["grp_s"], ex["grp_off"])
+    t2 = time.perf_counter()
+    cs = ref.combine_send(ws.N, ws.T, ws.E, ws.R, ws.H, cap, y, rc["expert_count"],
+                          rc["expert_send_off"], rc["send_off"], ex["seg_off"], ex["csend_off"])
+    ref.combine_recv(ws.N, ws.T, ws.E, ws.R, ws.H, cap, cs, d["topk_idx"], d["topk_w"],
+                     rc["slot_row"], rc["send_off"], ex["csend_off"])
+    t3 = time.perf_counter()
+    return t1 - t0, t3 - t2
+
+
+def _oracle_worker(timed: int) -> float:
+    from combine_expert_count_gb300 import workloads as W
+    w = W.CONFIGS["dsv3_decode"]
+    ws = w.replace(T=16, seed=w.seed + 17 + os.getpid() % 7)
+    d = W.generate(ws)
+    t0 = time.perf_counter()
+    if timed:
+        oracle_phases(ws, d)
+    return time.perf_counter() - t0
+
+
 def pairs_of(w, idx) -> int:
     """(token, expert rank) pairs: the rows the send-side reduction sends."""
     ranks = np.asarray(idx).reshape(w.N * w.T, w.R) // w.Er
@@ -414,6 +560,12 @@ def run_ours(args) -> None:
                                 buf.csend_off, buf.m_sizes, buf.status)
     fused_calls = (route, lambda: m.moe_dispatch_send_recv(sh, tens),
                    lambda: m.moe_combine(sh, tens))
+    # a1 and a2 as their own calls (the separate-call form of the route)
+    route_split = (
+        lambda: m.moe_route_count(sh, idx, buf.expert_count, buf.send_off, buf.expert_send_off,
+                                  buf.slot_row, buf.status),
+        lambda: m.moe_exchange(sh, buf.expert_count, buf.send_off, buf.grp_off, buf.seg_off,
+                               buf.csend_off, buf.m_sizes, buf.status))
     separate_calls = (
         route,
         lambda: m.moe_dispatch_send(sh, x, buf.slot_row, buf.send_q, buf.send_s, buf.send_tok,
@@ -508,6 +660,7 @@ def run_ours(args) -> None:
         # (3) per-kernel breakdowns: eager launches, an event after each call
         fused_k = time_kernels(fused_calls, K)
         sep_k = time_kernels(separate_calls, K)
+        rcx_k = time_kernels(route_split, K)
         # (4) end to end through the public API with host buffers in pinned
         # memory, all transfers inside the window: the router's ids and
         # weights are copied host -> device, the kernels read x from host
@@ -607,6 +760,10 @@ def run_ours(args) -> None:
     # the combine with send-side reduction on the same expert outputs
     partial = partial_combine_line(m, buf, w, d, x, idx, wt, tens, capture, time_steps,
                                    time_kernels, flush, K, W_, world)
+    others = None
+    if rank == 0 and not args.no_skew:
+        others = [config_line(m, W, name, dev, capture, flush, min(K, 20), W_)
+                  for name in ("kimi_k2_decode", "prefill")]
     if rank == 0 and not args.no_skew:
         skew = [skew_line(m, W, name, dev, capture, flush, K, W_)
                 for name in ("qwen3_zipf0", "qwen3_zipf0.5", "qwen3_zipf1", "qwen3_zipf1.5",
@@ -654,6 +811,8 @@ def run_ours(args) -> None:
         "signalled": signalled,
         "send_side_reduction": partial,
         "routing_skew": skew,
+        "other_configs": others,
+        "per_kernel": per_kernel_table(nbytes, favg, savg, rcx_k, A, w, args.config),
         "dispatch_us": round((favg["route"] + favg["dispatch_fused"]) * 1000, 2),
         "combine_us": round(favg["combine_fused"] * 1000, 2),
         "achieved_gbs": round(achieved, 1),
@@ -741,9 +900,13 @@ def main() -> None:
                     help="skip the skewed-routing (Zipf) layer lines")
     ap.add_argument("--profile-pass", action="store_true",
                     help="run every kernel twice without timing (for ncu) and exit")
+    ap.add_argument("--oracle-table", action="store_true",
+                    help="time the CPU oracle per configuration and phase, then exit")
     args = ap.parse_args()
     if args.profile_pass:
         profile_pass(args)
+    elif args.oracle_table:
+        oracle_table(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
