@@ -22,17 +22,6 @@ namespace moe {
 // k = 0..R-1, rounding once to bf16 at the end.
 constexpr int kReduceGroup = 8;  // row loads kept in flight per chunk
 
-// Store of one 16-byte vector of a row written once and not read back here.
-#ifndef MOE_STREAM_STORES
-#define MOE_STREAM_STORES 0
-#endif
-__device__ __forceinline__ void st_row(uint4 *p, const uint4 &v) {
-    if (MOE_STREAM_STORES)
-        __stcs(p, v);
-    else
-        *p = v;
-}
-
 // kLL: the rows come from the low-latency layout, row ll_row[s][t][k] of
 // `csend` (there y_ll), instead of the combine send buffers.
 template <bool kLL>
@@ -184,7 +173,7 @@ __global__ void __launch_bounds__(kGatherThreads)
 #pragma unroll
                 for (int u = 0; u < KR; ++u) {
                     if (cs[u]) {
-                        st_row(cs[u] + part, v[u]);
+                        cs[u][part] = v[u];
                         fma8(acc, wr[u], v[u]);
                     }
                 }
