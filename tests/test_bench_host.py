@@ -85,3 +85,28 @@ def test_max_over_ranks_gloo_two_ranks():
         assert p.exitcode == 0
     got = sorted(q.get(timeout=10) for _ in range(2))
     assert got == [(0, 11.0), (1, 11.0)]
+
+
+def test_per_kernel_table_ratios():
+    """Each kernel row carries its algorithmic GB/s; rows with a committed
+    DRAM record for the current source also carry DRAM GB/s and the
+    DRAM / algorithmic ratio; the routing kernels are marked latency-bound."""
+    w = W.CONFIGS["dsv3_decode"]
+    nb = bench.algorithmic_bytes(w, w.A)
+    favg = {"route": 0.010, "dispatch_fused": 0.050, "combine_fused": 0.085}
+    savg = {"route": 0.010, "dispatch_send": 0.030, "dispatch_recv": 0.042,
+            "combine_send": 0.083, "combine_recv": 0.039}
+    rows = bench.per_kernel_table(nb, favg, savg, [[0.01], [0.006]], w.A, w, "dsv3_decode")
+    by = {r["kernel"]: r for r in rows}
+    assert {"route_count", "exchange", "route", "dispatch_send", "dispatch_recv",
+            "combine_send", "combine_recv", "dispatch_fused", "combine_fused"} == set(by)
+    for k in ("route_count", "exchange", "route"):
+        assert by[k]["bound"] == "latency" and "algorithmic_gbs" not in by[k]
+    c = by["combine_fused"]
+    assert c["algorithmic_gbs"] == round(nb["fused"]["combine_fused"] / 85e-6 / 1e9, 1)
+    dram = bench.dram_traffic("combine_fused", "dsv3_decode")
+    if dram is None:
+        assert "dram_mb" not in c
+    else:
+        assert c["dram_over_algorithmic"] == round(dram / nb["fused"]["combine_fused"], 3)
+        assert 0.0 < c["dram_over_algorithmic"] <= 1.5
