@@ -309,3 +309,16 @@ def test_e4m3_encoder_matches_oracle_exhaustively():
     o = torch.empty(5, dtype=torch.uint8, device="cuda")
     m.moe_e4m3_encode(t, o)
     assert list(o.cpu().numpy()) == list(ref.e4m3_encode(v))
+
+
+@pytest.mark.parametrize("N,T,E,R,H", [(2, 9, 32, 12, 128), (2, 5, 64, 32, 256),
+                                       (3, 4, 24, 9, 384)])
+@pytest.mark.parametrize("calls", ["fused", "separate", "fused_route", "signalled"])
+def test_many_experts_per_token(N, T, E, R, H, calls):
+    """More than eight slots per token (the quantiser stores to every slot's
+    rows from registers; the combine's slot table leaves registers), every
+    output against the oracle."""
+    w = W.Workload("wide", N=N, T=T, H=H, E=E, R=R, seed=1000 + N * 10 + R)
+    d = W.generate(w)
+    G.compare_with_oracle(w, G.run_path(w, G.to_dev(d), calls=calls),
+                          _oracle(w, d, w.default_cap))
