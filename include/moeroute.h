@@ -57,12 +57,16 @@
  * Ownership: every pointer is device memory owned by the caller (sized with
  * moe_sizes_query), except that x and out may also be pinned host memory
  * (cudaHostAlloc / page-locked): the kernels then read x and write out
- * directly over the CPU-GPU link, with no separate copy.  The library allocates nothing and keeps no state
- * between calls.  `stream` is a cudaStream_t (NULL = legacy default stream).
+ * directly over the CPU-GPU link, with no separate copy.  The library
+ * allocates nothing and keeps no state between calls, apart from the fixed
+ * static scratch array that moe_dispatch_signalled_static uses instead of a
+ * caller buffer (see there).  `stream` is a cudaStream_t (NULL = legacy
+ * default stream).
  *
  * Execution: calls only enqueue work on `stream` and never wait for the
- * device, so a sequence of calls can be captured in a CUDA graph.  Order on
- * the stream replaces the pages' receive-side waits and barriers.
+ * device; sequences of the calls other than moe_dispatch_signalled_static can
+ * be captured in a CUDA graph (tested).  Order on the stream replaces the
+ * pages' receive-side waits and barriers.
  *
  * Errors: argument checks run on the host before anything is enqueued and
  * return MOE_EINVAL; a failed launch returns MOE_ECUDA.  Faults found on the
