@@ -141,6 +141,13 @@ def test_null_and_misaligned_pointers_rejected(lib):
                                         None) == m.MOE_EINVAL, field
     assert L.moe_expert_standin(ctypes.byref(sh), 2, good, good, good, good, None) == m.MOE_EINVAL
     assert L.moe_expert_standin(ctypes.byref(sh), 0, bad, good, good, good, None) == m.MOE_EINVAL
+    assert L.moe_expert_standin_ll(ctypes.byref(sh), 2, good, good, good, good,
+                                   None) == m.MOE_EINVAL
+    for i in range(4):
+        for p in (bad, null):
+            args = [good] * 4
+            args[i] = p
+            assert L.moe_expert_standin_ll(ctypes.byref(sh), 0, *args, None) == m.MOE_EINVAL
     assert L.moe_e4m3_encode(null, good, 4, None) == m.MOE_EINVAL
     assert L.moe_e4m3_encode(good, good, -1, None) == m.MOE_EINVAL
     assert L.moe_route_count(None, good, good, good, good, good, good, None) == m.MOE_EINVAL
