@@ -880,6 +880,34 @@ def profile_pass(args) -> None:
     print("profile pass done: 13 library launches per pass", flush=True)
 
 
+def profile_headline(args) -> None:
+    """The headline step only (moe_dispatch + moe_combine) eight times, L2
+    flushed before each, nothing timed: a launch list of exactly the kernels
+    the headline number times."""
+    import torch
+
+    from combine_expert_count_gb300 import moeroute as m
+    from combine_expert_count_gb300 import workloads as W
+
+    w = W.CONFIGS[args.config]
+    d = W.generate(w)
+    buf = m.MoeBuffers(w.N, w.T, w.E, w.R, w.H, cap=args.cap)
+    x = torch.from_numpy(d["x"].view(np.int16)).cuda()
+    idx = torch.from_numpy(d["topk_idx"]).cuda()
+    wt = torch.from_numpy(d["topk_w"]).cuda()
+    buf.dispatch(x, idx)
+    buf.expert(1 if w.expert == "scale" else 0)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    for _ in range(8):
+        flush.zero_()
+        buf.dispatch(x, idx)
+        buf.combine(idx, wt)
+    torch.cuda.synchronize()
+    if int(buf.status.item()) != 0:
+        raise RuntimeError(f"device status {int(buf.status.item())}")
+    print("headline profile pass done: 8 steps of 3 library launches", flush=True)
+
+
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -902,8 +930,12 @@ def main() -> None:
                     help="run every kernel twice without timing (for ncu) and exit")
     ap.add_argument("--oracle-table", action="store_true",
                     help="time the CPU oracle per configuration and phase, then exit")
+    ap.add_argument("--profile-headline", action="store_true",
+                    help="run only the headline step eight times without timing (for ncu)")
     args = ap.parse_args()
-    if args.profile_pass:
+    if args.profile_headline:
+        profile_headline(args)
+    elif args.profile_pass:
         profile_pass(args)
     elif args.oracle_table:
         oracle_table(args)
