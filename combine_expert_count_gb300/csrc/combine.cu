@@ -22,12 +22,12 @@ namespace moe {
 // k = 0..R-1, rounding once to bf16 at the end.
 constexpr int kReduceGroup = 8;  // row loads kept in flight per chunk
 // Blocks per token in the fused combine, each a contiguous half of every
-// row: 2 measured 84.6 us against 86.7 us with whole tokens on the DSv3 EP16
-// combine (finer work evens out the last wave of blocks); 4 or 8 were no
-// better.
-#ifndef MOE_COMB_SPLIT
-#define MOE_COMB_SPLIT 2
-#endif
+// row, when a half still gives every thread at least one 16-byte chunk per
+// row (H >= 4096 with 256 threads): on the DSv3 EP16 combine two blocks per
+// token measured 84.6 us against 86.7 us with whole tokens (finer work evens
+// out the last wave of blocks); 4 or 8 were no better; on H = 2048 rows the
+// split would leave half of every block idle.
+static int combine_split(int H) { return (H >> 3) >= 2 * kGatherThreads ? 2 : 1; }
 
 // kLL: the rows come from the low-latency layout, row ll_row[s][t][k] of
 // `csend` (there y_ll), instead of the combine send buffers.
@@ -126,7 +126,8 @@ cudaError_t launch_combine_ll(const moe_shape &sh, const uint16_t *y_ll, const f
 // position was dropped is written as zeros and contributes w * 0.
 template <int KR>  // 0: slots read from shared memory; else R <= KR slots held in registers
 __global__ void __launch_bounds__(kGatherThreads)
-    k_combine_fused(int N, int T, int E, int R, int H, int cap, const uint16_t *__restrict__ y,
+    k_combine_fused(int N, int T, int E, int R, int H, int cap, int split,
+                    const uint16_t *__restrict__ y,
                     const int32_t *__restrict__ idx, const float *__restrict__ w,
                     const int32_t *__restrict__ slot_row, const int32_t *__restrict__ eso,
                     const int32_t *__restrict__ seg_off, const int32_t *__restrict__ send_off,
@@ -137,8 +138,8 @@ __global__ void __launch_bounds__(kGatherThreads)
     __shared__ float wk[MOE_MAX_TOPK];
     const int Er = E / N, cpr = H >> 3;
     const long long ntok = (long long)N * T;
-    // MOE_COMB_SPLIT blocks share a token, each a contiguous part of its rows
-    const int split = MOE_COMB_SPLIT, per = (cpr + split - 1) / split;
+    // `split` blocks share a token, each a contiguous part of its rows
+    const int per = (cpr + split - 1) / split;
     for (long long blk = blockIdx.x; blk < ntok * split; blk += gridDim.x) {
         const long long tok = blk / split;
         const int c0 = (int)(blk - tok * split) * per, c1 = min(cpr, c0 + per);
@@ -235,12 +236,13 @@ cudaError_t launch_combine_fused(const moe_shape &sh, int cap, const uint16_t *y
                                  uint16_t *csend, uint16_t *out, cudaStream_t st) {
     const long long ntok = (long long)sh.N * sh.T;
     if (ntok <= 0) return cudaSuccess;
-    const long long nblk = ntok * MOE_COMB_SPLIT;
+    const int split = combine_split(sh.H);
+    const long long nblk = ntok * split;
     const int grid = (int)(nblk < (1LL << 30) ? nblk : (1LL << 30));
     auto kern = sh.R <= 8 ? k_combine_fused<8> : k_combine_fused<0>;
     return launch_kernel(kern, dim3((unsigned)grid), dim3(kGatherThreads), 0, st, sh.N, sh.T, sh.E,
-                         sh.R, sh.H, cap, y, idx, w, slot_row, eso, seg_off, send_off, csend_off,
-                         csend, out);
+                         sh.R, sh.H, cap, split, y, idx, w, slot_row, eso, seg_off, send_off,
+                         csend_off, csend, out);
 }
 
 // ------------------------------------------------------------ expert stand-in
