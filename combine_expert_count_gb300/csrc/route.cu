@@ -3,10 +3,10 @@
 // and receive buffers" and "Dispatch and combine").
 //
 // k_route_count: one 1024-thread block per rank, as the page describes
-//   (counts accumulated with shared-memory atomics inside a single block,
-//   then a cumulative sum), and the stable slot of every (t, k) (see
-//   route_sender).  The result equals "expert offset + number of earlier
-//   assignments with the same expert", independent of atomic order.
+//   (counts accumulated in shared memory inside a single block, then a
+//   cumulative sum), and the stable slot of every (t, k) (see route_sender).
+//   Each warp counts into a shared-memory table row of its own, so the counts
+//   need no atomics, and the slots follow from the same tables.
 //
 // k_exchange: one block per receiver; a block scan over the Er*N counts in
 //   (local expert, sender) order gives seg_off / grp_off / m_sizes, and a
@@ -18,31 +18,33 @@ namespace moe {
 
 constexpr int kRouteThreads = 1024;
 
-// Shared memory of the sender role: cnt, base, run ([E] ints each) and a
-// stamped (warp x expert) table of 32-bit entries.
-static size_t route_smem(int E) { return (size_t)E * 3 * sizeof(int) + (size_t)E * 32 * 4; }
+// Shared memory of the sender role: base ([E] ints) and the per-warp count
+// table ([32 warps][E] ints).
+static size_t route_smem(int E) { return (size_t)E * 33 * sizeof(int); }
 
 // Sender role of rank s = blockIdx.x: counts, scans and stable slots.
 // Returns (the same in every thread) whether an id was outside [0, E); the
 // caller raises MOE_ST_BAD_EXPERT.
 //
-// Stable slots, one chunk of blockDim.x assignments at a time: a lane's rank
-// among equal experts in its warp comes from __match_any_sync; the count of
-// the same expert in earlier warps of the chunk from a (warp x expert)
-// table in which each warp's leader stores (chunk stamp << 16 | count);
-// entries with another chunk's stamp read as zero, so the table is never
-// cleared.  run[e] carries earlier chunks.
+// Stable slots in three passes, whatever T*R is: (1) warp w walks its own
+// contiguous share of the rank's ids, 32 at a time; lanes holding the same
+// expert find each other with __match_any_sync, the group's first lane adds
+// the group to the warp's running count of that expert (a table row of its
+// own, so no block barrier is needed) and every lane keeps "running count
+// before its group + its rank in the group" -- its rank among equal ids in
+// the warp's share -- in slot_row for now; (2) per expert, the warps' counts
+// become an exclusive prefix over warps, and their sum the expert's count,
+// whose exclusive scan gives the send offsets; (3) each lane adds its
+// expert's offset and its warp's prefix.  The result equals "expert offset +
+// number of earlier assignments with the same expert".
 __device__ __forceinline__ bool route_sender(int N, int T, int E, int R,
                                              const int32_t *__restrict__ idx,
                                              int32_t *__restrict__ cnt_out,
                                              int32_t *__restrict__ send_off,
                                              int32_t *__restrict__ eso_out,
-                                             int32_t *__restrict__ slot_row,
-                                             int *smem) {
-    int *cnt = smem;      // [E] counts
-    int *base = cnt + E;  // [E] exclusive scan of counts
-    int *run = base + E;  // [E] assignments seen in earlier chunks
-    uint32_t *tab = reinterpret_cast<uint32_t *>(run + E);  // [32 warps][E]
+                                             int32_t *__restrict__ slot_row, int *smem) {
+    int *base = smem;     // [E] exclusive scan of counts
+    int *tab = base + E;  // [nw][E] warp counts, then their exclusive prefix over warps
     __shared__ int wsum[32];
     __shared__ int total;
     __syncthreads();  // callers may reuse shared memory around this
@@ -51,28 +53,45 @@ __device__ __forceinline__ bool route_sender(int N, int T, int E, int R,
     const int nw = blockDim.x >> 5;
     const int TR = T * R, Er = E / N;
     const int32_t *id = idx + (size_t)s * TR;
+    int32_t *srow = slot_row + (size_t)s * TR;
 
-    for (int e = tid; e < E; e += blockDim.x) {
-        cnt[e] = 0;
-        run[e] = 0;
-    }
     for (int i = tid; i < nw * E; i += blockDim.x) tab[i] = 0;
     __syncthreads();
 
-    // 1. counts with shared-memory atomics
+    // 1. each warp's share: rank among equal ids, running counts per expert
+    const int per = (TR + nw - 1) / nw;
+    const int lo = min(TR, warp * per), hi = min(TR, lo + per);
+    int *mytab = tab + warp * E;
+    const unsigned lt = (1u << lane) - 1u;
     int bad = 0;
-    for (int i = tid; i < TR; i += blockDim.x) {
-        int e = __ldg(id + i);
-        if ((unsigned)e < (unsigned)E)
-            atomicAdd(&cnt[e], 1);
-        else
-            bad = 1;
+    for (int r0 = lo; r0 < hi; r0 += 32) {
+        const int i = r0 + lane;
+        const int e = i < hi ? __ldg(id + i) : -1;
+        const bool good = (unsigned)e < (unsigned)E;
+        if (i < hi && !good) bad = 1;
+        const unsigned peers = __match_any_sync(kFull, good ? e : -1);
+        const int leader = __ffs(peers) - 1;
+        int before = 0;
+        if (good && lane == leader) {
+            before = mytab[e];
+            mytab[e] = before + __popc(peers);
+        }
+        before = __shfl_sync(kFull, before, leader);
+        if (i < hi) srow[i] = good ? before + __popc(peers & lt) : -1;
+        __syncwarp();
     }
     const bool any_bad = __syncthreads_or(bad) != 0;
 
-    // 2. exclusive scan over experts (E <= blockDim.x: one expert per thread)
-    int v = tid < E ? cnt[tid] : 0;
-    int incl = block_inclusive_scan(v, wsum, &total);
+    // 2. counts, prefix over warps, exclusive scan over experts
+    int v = 0;
+    if (tid < E) {
+        for (int w = 0; w < nw; ++w) {
+            const int c = tab[w * E + tid];
+            tab[w * E + tid] = v;
+            v += c;
+        }
+    }
+    const int incl = block_inclusive_scan(v, wsum, &total);
     if (tid < E) {
         base[tid] = incl - v;
         cnt_out[(size_t)s * E + tid] = v;
@@ -83,45 +102,12 @@ __device__ __forceinline__ bool route_sender(int N, int T, int E, int R,
     for (int p = tid; p <= N; p += blockDim.x)
         send_off[(size_t)s * (N + 1) + p] = p < N ? base[p * Er] : total;
 
-    // 3. stable slots
-    const unsigned lt = (1u << lane) - 1u;
-    for (int c0 = 0, chunk = 0; c0 < TR; c0 += blockDim.x, ++chunk) {
-        const uint32_t stamp = (uint32_t)(chunk % 65535) + 1u;
-        if (chunk > 0 && stamp == 1u) {  // stamps wrap every 65535 chunks: clear once
-            for (int i = tid; i < nw * E; i += blockDim.x) tab[i] = 0;
-            __syncthreads();
-        }
-        const int i = c0 + tid;
-        const int e = i < TR ? __ldg(id + i) : -1;
-        const bool good = (unsigned)e < (unsigned)E;
-        const unsigned peers = __match_any_sync(kFull, good ? e : -1);
-        const int rank = __popc(peers & lt);
-        if (good && rank == 0) tab[warp * E + e] = (stamp << 16) | (uint32_t)__popc(peers);
-        __syncthreads();
-        if (i < TR) {
-            int slot = -1;
-            if (good) {
-                int pre = 0;
-#pragma unroll 8
-                for (int w2 = 0; w2 < warp; ++w2) {
-                    const uint32_t t = tab[w2 * E + e];
-                    pre += (t >> 16) == stamp ? (int)(t & 0xffffu) : 0;
-                }
-                slot = base[e] + run[e] + pre + rank;
-            }
-            slot_row[(size_t)s * TR + i] = slot;
-        }
-        if (c0 + (int)blockDim.x < TR) {  // carry this chunk's counts to the next
-            __syncthreads();
-            for (int x = tid; x < E; x += blockDim.x) {
-                int add = 0;
-                for (int w2 = 0; w2 < nw; ++w2) {
-                    const uint32_t t = tab[w2 * E + x];
-                    add += (t >> 16) == stamp ? (int)(t & 0xffffu) : 0;
-                }
-                run[x] += add;
-            }
-            __syncthreads();
+    // 3. slots (each lane revisits the ids it ranked in pass 1)
+    for (int r0 = lo; r0 < hi; r0 += 32) {
+        const int i = r0 + lane;
+        if (i < hi) {
+            const int e = __ldg(id + i);
+            if ((unsigned)e < (unsigned)E) srow[i] = base[e] + tab[warp * E + e] + srow[i];
         }
     }
     return any_bad;
