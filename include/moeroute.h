@@ -143,8 +143,9 @@ typedef struct {
 /* Fill *out for *shape.  Host only.  MOE_EINVAL / MOE_ENOTSUP on a bad shape. */
 int moe_sizes_query(const moe_shape *shape, moe_sizes *out);
 
-/* Dispatch send, step 1 ("Dispatch and combine": per-expert counts with
- * shared-memory atomics in one block per rank, then a cumulative sum).
+/* Dispatch send, step 1 ("Dispatch and combine": per-expert counts in one
+ * block per rank -- shared-memory atomics on the page, per-warp shared-memory
+ * tables here, with the same counts -- then a cumulative sum).
  * Clears *status.  One thread block per rank s:
  *   expert_count[s][e]   = #{(t,k): topk_idx[s][t][k] == e}
  *   expert_send_off[s][] = exclusive scan of expert_count[s][] (E+1 entries)
