@@ -99,10 +99,11 @@ def test_ll_output_equals_main_path():
 @pytest.mark.parametrize("N,T,E,R,H", [(1, 5, 4, 2, 128), (2, 16, 8, 3, 256), (3, 7, 6, 2, 384),
                                        (4, 33, 16, 4, 640), (2, 3, 4, 2, 8192 + 1024),
                                        (2, 9, 32, 12, 128), (2, 5, 64, 32, 256),
-                                       (2, 1024, 8, 2, 128)])
+                                       (2, 1024, 8, 2, 128), (4, 8, 1024, 32, 128)])
 def test_ll_small_shapes(N, T, E, R, H):
     """Includes more than eight slots per token (the earlier-id count runs in
-    groups of eight), 32 slots, and the longest batch (T = 1024)."""
+    groups of eight), 32 slots, the longest batch (T = 1024) and the most
+    experts (1024, the largest region-count histogram)."""
     w = W.Workload("llgrid", N=N, T=T, H=H, E=E, R=R, seed=N * 100 + T)
     d = W.generate(w)
     b = _run_ll(w, d, 0)
