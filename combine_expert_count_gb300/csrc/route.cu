@@ -11,6 +11,8 @@
 // k_exchange: one block per receiver; a block scan over the Er*N counts in
 //   (local expert, sender) order gives seg_off / grp_off / m_sizes, and a
 //   second scan over senders gives csend_off.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -261,6 +263,9 @@ cudaError_t launch_route_count(const moe_shape &sh, const int32_t *idx, int32_t 
 // through L2 -- the routing-information exchange of the pages, between the
 // SMs of one cluster.  Block 0 clears *status before the barrier and every
 // status bit is raised after it, so no separate clear precedes the launch.
+// kGrid: the same for more ranks than a cluster holds, as a cooperative
+// launch (every block resident) meeting at a grid-wide barrier instead.
+template <bool kGrid>
 __global__ void __launch_bounds__(kRouteThreads, 1)
     k_route_cluster(int N, int T, int E, int R, int cap, const int32_t *__restrict__ idx,
                     int32_t *__restrict__ cnt_out, int32_t *__restrict__ send_off,
@@ -271,8 +276,12 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     extern __shared__ int smem[];
     if (blockIdx.x == 0 && threadIdx.x == 0) *status = 0;
     const bool bad = route_sender(N, T, E, R, idx, cnt_out, send_off, eso_out, slot_row, smem);
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    if constexpr (kGrid) {
+        cooperative_groups::this_grid().sync();
+    } else {
+        asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+        asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    }
     const int r = blockIdx.x, tid = threadIdx.x, Er = E / N, F = Er * N;
     if (bad && tid == 0) flag(status, MOE_ST_BAD_EXPERT);
     const int j = tid / N, s = tid - (tid / N) * N;
@@ -292,9 +301,9 @@ static int route_cluster_limit(int E) {
     if (dev == cached_dev) return cached;
     cached_dev = dev;
     cached = 0;
-    if (cudaFuncSetAttribute(k_route_cluster, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+    if (cudaFuncSetAttribute(k_route_cluster<false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
             cudaSuccess ||
-        cudaFuncSetAttribute(k_route_cluster, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(k_route_cluster<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)route_smem(MOE_MAX_EXPERTS)) != cudaSuccess) {
         cudaGetLastError();
         return 0;
@@ -312,12 +321,34 @@ static int route_cluster_limit(int E) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, k_route_cluster, &cfg) == cudaSuccess && n >= 1) {
+        if (cudaOccupancyMaxActiveClusters(&n, k_route_cluster<false>, &cfg) == cudaSuccess &&
+            n >= 1) {
             cached = c;
             break;
         }
         cudaGetLastError();
     }
+    return cached;
+}
+
+// Most ranks whose route blocks can all be resident at once (0: none).
+static int route_grid_limit(int E) {
+    static int cached_dev = -1, cached_e = -1, cached = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev == cached_dev && E == cached_e) return cached;
+    cached_dev = dev;
+    cached_e = E;
+    cached = 0;
+    int occ = 0;
+    if (cudaFuncSetAttribute(k_route_cluster<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)route_smem(MOE_MAX_EXPERTS)) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_route_cluster<true>, kRouteThreads,
+                                                      route_smem(E)) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cached = occ * sm_count();
     return cached;
 }
 
@@ -349,10 +380,15 @@ cudaError_t launch_route(const moe_shape &sh, int cap, const int32_t *idx, int32
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         // the kernel clears *status itself
-        return cudaLaunchKernelEx(&cfg, k_route_cluster, sh.N, sh.T, sh.E, sh.R, cap, idx, cnt,
-                                  send_off, eso, slot_row, grp_off, seg_off, csend_off, m_sizes,
-                                  status);
+        return cudaLaunchKernelEx(&cfg, k_route_cluster<false>, sh.N, sh.T, sh.E, sh.R, cap, idx,
+                                  cnt, send_off, eso, slot_row, grp_off, seg_off, csend_off,
+                                  m_sizes, status);
     }
+    if (sh.N > 1 && sh.N <= route_grid_limit(sh.E))  // clears *status itself too
+        return launch_kernel_coresident(k_route_cluster<true>, dim3(sh.N), dim3(kRouteThreads),
+                                        route_smem(sh.E), st, sh.N, sh.T, sh.E, sh.R, cap, idx,
+                                        cnt, send_off, eso, slot_row, grp_off, seg_off,
+                                        csend_off, m_sizes, status);
     err = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
     if (err != cudaSuccess) return err;
     k_route<<<sh.N, kRouteThreads, route_smem(sh.E), st>>>(sh.N, sh.T, sh.E, sh.R, cap, idx, cnt,
