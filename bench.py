@@ -840,7 +840,8 @@ def run_ours(args) -> None:
         "wall_s_timed": round(t_wall, 3),
     }
     if world == 1 and not args.no_cpu_baseline:
-        v, sample, spent = oracle_layer_us(w, max(1, min(w.T, args.ref_tokens)), args.cpu_seconds)
+        v, sample, spent = oracle_layer_us(w, max(1, min(w.T, args.ref_tokens)), args.cpu_seconds,
+                                           max_reps=1000)
         line["cpu_baseline"] = {"value": round(v, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
                                 "sample": sample, "cpu_seconds": round(spent, 1)}
     print(json.dumps(line), flush=True)
