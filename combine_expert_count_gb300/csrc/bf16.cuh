@@ -22,8 +22,11 @@ namespace moe {
 // blocks.  Kernels that also write every row they read (moe_combine, the
 // sending side of the send-side reduction) use 256, each step covering a
 // 4 KB stretch of every row: on the DSv3 EP16 combine that measured 86.7 us
-// against 90.8 us with 64 threads (192, 384 and 512 were no better), while
-// the read-only reduce measured 39.4 us with 64 threads and 44.9 us with 256.
+// against 90.8 us with 64 threads (192, 384 and 512 were no better; with
+// two blocks per token, 160, 224 and 448 measured 86.7, 84.6 and 94.9 us
+// against 84.6, and 224 made the sending side of the send-side reduction
+// 2 us slower), while the read-only reduce measured 39.4 us with 64 threads
+// and 44.9 us with 256.
 constexpr int kReduceThreads = MOE_REDUCE_THREADS;
 constexpr int kGatherThreads = MOE_GATHER_THREADS;
 
