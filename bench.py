@@ -107,12 +107,43 @@ KERNEL_SOURCES = {
 }
 
 
-def source_hash(kernel: str) -> str:
-    h = hashlib.sha256()
+def code_only(src: str) -> str:
+    """C/C++ source with comments removed and whitespace runs collapsed, so
+    that a comment edit leaves the hash alone while any code edit changes it.
+    String and character literals are kept whole."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def source_hash(kernel: str, read=None) -> str:
+    """Hash of the code (comments and whitespace aside) of a kernel's sources;
+    ``read(name)`` returns a source's text (default: the working tree)."""
     csrc = os.path.join(ROOT, "combine_expert_count_gb300", "csrc")
+    if read is None:
+        def read(f):
+            with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+                return fh.read()
+    h = hashlib.sha256()
     for f in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        h.update((f + "\n" + code_only(read(f))).encode())
     return h.hexdigest()[:16]
 
 

@@ -110,3 +110,19 @@ def test_per_kernel_table_ratios():
     else:
         assert c["dram_over_algorithmic"] == round(dram / nb["fused"]["combine_fused"], 3)
         assert 0.0 < c["dram_over_algorithmic"] <= 1.5
+
+
+def test_traffic_record_follows_code_not_comments():
+    src = bench.KERNEL_SOURCES["combine_fused"]
+    csrc = os.path.join(ROOT, "combine_expert_count_gb300", "csrc")
+    text = {f: open(os.path.join(csrc, f), encoding="utf-8").read() for f in src}
+    base = bench.source_hash("combine_fused", read=lambda f: text[f])
+    assert base == bench.source_hash("combine_fused")
+    commented = dict(text)
+    commented[src[0]] = "// a new comment\n/* and a block\n comment */" + \
+        text[src[0]].replace("\n", "  \n", 3)
+    assert bench.source_hash("combine_fused", read=lambda f: commented[f]) == base
+    changed = dict(text)
+    changed[src[0]] = text[src[0]] + "\nstatic int extra_code = 1;\n"
+    assert bench.source_hash("combine_fused", read=lambda f: changed[f]) != base
+    assert bench.code_only('x = "// kept"; // dropped\ny') == 'x = "// kept"; y'
