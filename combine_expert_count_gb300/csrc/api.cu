@@ -1,7 +1,9 @@
 // api.cu -- the extern "C" boundary of libmoeroute: argument validation on
 // the host, then asynchronous launches on the caller's stream.  Nothing here
 // allocates device memory, synchronises the host or keeps state between
-// calls, except the per-device SM count cache.
+// calls, except per-device caches of launch properties (SM count here,
+// occupancies and cluster limits beside each launcher).
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 
@@ -11,14 +13,17 @@
 namespace moe {
 
 int sm_count() {
-    static int cached[64] = {0};
+    static std::atomic<int> cached[64];  // zero-initialised: not yet asked
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
-    if (dev < 64 && cached[dev] > 0) return cached[dev];
+    if (dev < 64) {
+        const int c = cached[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
     int n = 1;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
         n = 1;
-    if (dev < 64) cached[dev] = n;
+    if (dev < 64) cached[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 

@@ -444,24 +444,20 @@ static cudaError_t launch_staged_x(const moe_shape &sh, const uint16_t *x,
     const int P = sh.H < kPieceElems ? sh.H : kPieceElems;
     const long long nitems = ntok * ((sh.H + P - 1) / P);
     const int threads = quant_threads(P / 16);
-    const int smem = (int)stage_bytes(P) + 128 +
-                     (kDest == Dest::kLowLatency ? MOE_MAX_EXPERTS * 4 : 0);
-    static int cached_dev = -1, cached_smem = -1, cached_threads = -1, cached_occ = 1;
-    int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
+    constexpr int kHist = kDest == Dest::kLowLatency ? MOE_MAX_EXPERTS * 4 : 0;
+    const int smem = (int)stage_bytes(P) + 128 + kHist;
+    static LaunchMemo memo;
+    int occ = 1;
+    cudaError_t err = memo.get(((long long)smem << 16) | threads, &occ, [&](int *v) {
+        // the attribute allows the largest piece, whatever this call's P
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)stage_bytes(kPieceElems) + 128 + kHist);
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(v, kern, threads, smem);
+        if (*v < 1) *v = 1;
+        return e;
+    });
     if (err != cudaSuccess) return err;
-    if (dev != cached_dev || smem != cached_smem || threads != cached_threads) {
-        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (err != cudaSuccess) return err;
-        int occ = 0;
-        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
-        if (err != cudaSuccess) return err;
-        cached_occ = occ < 1 ? 1 : occ;
-        cached_dev = dev;
-        cached_smem = smem;
-        cached_threads = threads;
-    }
-    long long grid = (long long)sm_count() * cached_occ;
+    long long grid = (long long)sm_count() * occ;
     if (grid > nitems) grid = nitems;
     return launch_kernel(kern, dim3((unsigned)grid), dim3(threads), (size_t)smem, st, sh.T, sh.R,
                          sh.H, P, 0LL, nitems, x, slot_row, send_q, send_s, send_tok, status, gd,
@@ -520,23 +516,18 @@ static cudaError_t launch_signalled_x(const moe_shape &sh, int cap, const uint16
     const long long nitems = (long long)sh.N * sh.T * npieces;
     const int threads = quant_threads(P / 16);
     const int smem = (int)stage_bytes(P) + 128;
-    static int cached_dev = -1, cached_smem = -1, cached_threads = -1, cached_occ = 1;
-    int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
+    static LaunchMemo memo;
+    int occ = 1;
+    cudaError_t err = memo.get(((long long)smem << 16) | threads, &occ, [&](int *v) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)stage_bytes(kPieceElems) + 128);
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(v, kern, threads, smem);
+        if (*v < 1) *v = 1;
+        return e;
+    });
     if (err != cudaSuccess) return err;
-    if (dev != cached_dev || smem != cached_smem || threads != cached_threads) {
-        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (err != cudaSuccess) return err;
-        int occ = 0;
-        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
-        if (err != cudaSuccess) return err;
-        cached_occ = occ < 1 ? 1 : occ;
-        cached_dev = dev;
-        cached_smem = smem;
-        cached_threads = threads;
-    }
     // every CTA resident at once: rows wait on groups other CTAs pack
-    long long grid = (long long)sm_count() * cached_occ;
+    long long grid = (long long)sm_count() * occ;
     if (grid > nitems) grid = nitems;
     const int N = sh.N;
     Signal sg;

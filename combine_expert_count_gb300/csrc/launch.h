@@ -5,6 +5,9 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include <mutex>
+#include <vector>
+
 #include "moeroute.h"
 
 namespace moe {
@@ -107,5 +110,41 @@ cudaError_t launch_e4m3_encode(const float *v, uint8_t *out, int64_t n, cudaStre
 
 // SM count of the current device (cached per device).
 int sm_count();
+
+// A launch property of the current device (a kernel's occupancy, a cluster
+// limit) worked out by `fill` once per (device, key) and kept.  The lookup
+// and `fill` run under one lock: host threads calling at once neither race
+// on the table nor launch before the attribute calls another thread makes
+// inside `fill` have finished.  A failed `fill` is not kept.
+class LaunchMemo {
+  public:
+    template <class F>
+    cudaError_t get(long long key, int *out, F &&fill) {
+        int dev = 0;
+        cudaError_t err = cudaGetDevice(&dev);
+        if (err != cudaSuccess) return err;
+        std::lock_guard<std::mutex> lock(mu_);
+        for (const Entry &e : entries_)
+            if (e.dev == dev && e.key == key) {
+                *out = e.value;
+                return cudaSuccess;
+            }
+        int v = 0;
+        err = fill(&v);
+        if (err != cudaSuccess) return err;
+        entries_.push_back(Entry{dev, key, v});
+        *out = v;
+        return cudaSuccess;
+    }
+
+  private:
+    struct Entry {
+        int dev;
+        long long key;
+        int value;
+    };
+    std::mutex mu_;
+    std::vector<Entry> entries_;
+};
 
 }  // namespace moe

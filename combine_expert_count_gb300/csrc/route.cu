@@ -240,17 +240,14 @@ cudaError_t launch_route_count(const moe_shape &sh, const int32_t *idx, int32_t 
     cudaError_t err = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
     if (err != cudaSuccess) return err;
     const size_t smem = route_smem(sh.E);
-    static int attr_dev = -1;
-    int dev = 0;
-    err = cudaGetDevice(&dev);
+    static LaunchMemo attr;  // room for the largest E, once per device
+    int set = 0;
+    err = attr.get(0, &set, [](int *v) {
+        *v = 1;
+        return cudaFuncSetAttribute(k_route_count, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)route_smem(MOE_MAX_EXPERTS));
+    });
     if (err != cudaSuccess) return err;
-    if (dev != attr_dev) {
-        // room for the largest E once per device
-        err = cudaFuncSetAttribute(k_route_count, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)route_smem(MOE_MAX_EXPERTS));
-        if (err != cudaSuccess) return err;
-        attr_dev = dev;
-    }
     k_route_count<<<sh.N, kRouteThreads, smem, st>>>(sh.N, sh.T, sh.E, sh.R, idx, cnt, send_off,
                                                      eso, slot_row, status);
     return cudaGetLastError();
@@ -293,79 +290,79 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     route_receiver(N, E, cap, v, w, grp_off, seg_off, csend_off, m_sizes, status);
 }
 
-// Largest cluster k_route_cluster can be launched with on this device (0: none).
+// Largest cluster k_route_cluster can be launched with on this device for E
+// experts (0: none).
 static int route_cluster_limit(int E) {
-    static int cached_dev = -1, cached = 0;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (dev == cached_dev) return cached;
-    cached_dev = dev;
-    cached = 0;
-    if (cudaFuncSetAttribute(k_route_cluster<false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(k_route_cluster<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)route_smem(MOE_MAX_EXPERTS)) != cudaSuccess) {
-        cudaGetLastError();
-        return 0;
-    }
-    for (int c = 16; c >= 2; c >>= 1) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(c);
-        cfg.blockDim = dim3(kRouteThreads);
-        cfg.dynamicSmemBytes = route_smem(E);
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = c;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, k_route_cluster<false>, &cfg) == cudaSuccess &&
-            n >= 1) {
-            cached = c;
-            break;
+    static LaunchMemo memo;
+    int limit = 0;
+    const cudaError_t err = memo.get(E, &limit, [&](int *v) {
+        *v = 0;
+        if (cudaFuncSetAttribute(k_route_cluster<false>,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess ||
+            cudaFuncSetAttribute(k_route_cluster<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)route_smem(MOE_MAX_EXPERTS)) != cudaSuccess) {
+            cudaGetLastError();
+            return cudaSuccess;
         }
-        cudaGetLastError();
-    }
-    return cached;
+        for (int c = 16; c >= 2; c >>= 1) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(c);
+            cfg.blockDim = dim3(kRouteThreads);
+            cfg.dynamicSmemBytes = route_smem(E);
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = c;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, k_route_cluster<false>, &cfg) == cudaSuccess &&
+                n >= 1) {
+                *v = c;
+                break;
+            }
+            cudaGetLastError();
+        }
+        return cudaSuccess;
+    });
+    return err == cudaSuccess ? limit : 0;
 }
 
 // Most ranks whose route blocks can all be resident at once (0: none).
 static int route_grid_limit(int E) {
-    static int cached_dev = -1, cached_e = -1, cached = 0;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (dev == cached_dev && E == cached_e) return cached;
-    cached_dev = dev;
-    cached_e = E;
-    cached = 0;
-    int occ = 0;
-    if (cudaFuncSetAttribute(k_route_cluster<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)route_smem(MOE_MAX_EXPERTS)) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_route_cluster<true>, kRouteThreads,
-                                                      route_smem(E)) != cudaSuccess) {
-        cudaGetLastError();
-        return 0;
-    }
-    cached = occ * sm_count();
-    return cached;
+    static LaunchMemo memo;
+    int limit = 0;
+    const cudaError_t err = memo.get(E, &limit, [&](int *v) {
+        int occ = 0;
+        *v = 0;
+        if (cudaFuncSetAttribute(k_route_cluster<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)route_smem(MOE_MAX_EXPERTS)) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_route_cluster<true>,
+                                                          kRouteThreads,
+                                                          route_smem(E)) != cudaSuccess) {
+            cudaGetLastError();
+            return cudaSuccess;
+        }
+        *v = occ * sm_count();
+        return cudaSuccess;
+    });
+    return err == cudaSuccess ? limit : 0;
 }
 
 cudaError_t launch_route(const moe_shape &sh, int cap, const int32_t *idx, int32_t *cnt,
                          int32_t *send_off, int32_t *eso, int32_t *slot_row, int32_t *grp_off,
                          int32_t *seg_off, int32_t *csend_off, int32_t *m_sizes, int32_t *status,
                          cudaStream_t st) {
-    static int attr_dev = -1;
-    int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
+    static LaunchMemo attr;
+    int set = 0;
+    cudaError_t err = attr.get(0, &set, [](int *v) {
+        *v = 1;
+        return cudaFuncSetAttribute(k_route, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)route_smem(MOE_MAX_EXPERTS));
+    });
     if (err != cudaSuccess) return err;
-    if (dev != attr_dev) {
-        err = cudaFuncSetAttribute(k_route, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)route_smem(MOE_MAX_EXPERTS));
-        if (err != cudaSuccess) return err;
-        attr_dev = dev;
-    }
     if (sh.N > 1 && sh.N <= route_cluster_limit(sh.E)) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(sh.N);

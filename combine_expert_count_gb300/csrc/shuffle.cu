@@ -74,18 +74,15 @@ static cudaError_t launch_copy(const Map &m, long long row0, long long nrows,
                                cudaStream_t st) {
     if (nrows <= 0) return cudaSuccess;
     auto kern = k_row_copy<U, Map>;
-    static int cached_dev = -1, cached_occ = 1;
-    int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
+    static LaunchMemo memo;
+    int occ = 1;
+    cudaError_t err = memo.get(0, &occ, [&](int *v) {
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(v, kern, 256, 0);
+        if (*v < 1) *v = 1;
+        return e;
+    });
     if (err != cudaSuccess) return err;
-    if (dev != cached_dev) {
-        int occ = 0;
-        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 256, 0);
-        if (err != cudaSuccess) return err;
-        cached_occ = occ < 1 ? 1 : occ;
-        cached_dev = dev;
-    }
-    long long warps = (long long)sm_count() * cached_occ * 8;
+    long long warps = (long long)sm_count() * occ * 8;
     if (warps > nrows) warps = nrows;
     const long long per = (nrows + warps - 1) / warps;
     warps = (nrows + per - 1) / per;

@@ -60,8 +60,10 @@
  * directly over the CPU-GPU link, with no separate copy.  The library
  * allocates nothing and keeps no state between calls, apart from the fixed
  * static scratch array that moe_dispatch_signalled_static uses instead of a
- * caller buffer (see there).  `stream` is a cudaStream_t (NULL = legacy
- * default stream).
+ * caller buffer (see there) and host-side caches of launch properties per
+ * device (SM count, occupancy, cluster limits; filled on a device's first
+ * call, under a lock, so host threads may call at once, each with its own
+ * buffers).  `stream` is a cudaStream_t (NULL = legacy default stream).
  *
  * Execution: calls only enqueue work on `stream` and never wait for the
  * device; sequences of the calls other than moe_dispatch_signalled_static can
