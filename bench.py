@@ -940,6 +940,87 @@ def profile_headline(args) -> None:
     print("headline profile pass done: 8 steps of 3 library launches", flush=True)
 
 
+def token_sweep(args) -> None:
+    """Layer time against tokens per rank on one configuration's shape: the
+    fused calls (moe_dispatch + moe_combine) and the low-latency calls, each a
+    CUDA-graph replay with L2 flushed before every step; one JSON line.  The
+    low-latency layout holds N*E*T rows, so it runs up to --sweep-ll-max."""
+    import torch
+
+    from combine_expert_count_gb300 import moeroute as m
+    from combine_expert_count_gb300 import workloads as W
+
+    base = W.CONFIGS[args.config]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    m.lib()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    K, W_ = args.steps, max(args.warmup, 3)
+    mode = 1 if base.expert == "scale" else 0
+
+    def capture(fn):
+        cs = torch.cuda.Stream(device=dev)
+        cs.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cs):
+            fn()
+        torch.cuda.synchronize()
+        return g.replay
+
+    def mean_us(once):
+        for _ in range(W_):
+            flush.zero_()
+            once()
+        evs = []
+        for _ in range(K):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            once()
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        return round(statistics.mean(a.elapsed_time(b) for a, b in evs) * 1000, 2)
+
+    rows = []
+    with ClockSampler(gpu_id(0)) as clk:
+        for T in args.sweep_tokens:
+            w = base.replace(T=T, seed=base.seed + 1000 + T)
+            d = W.generate(w)
+            b = m.MoeBuffers(w.N, w.T, w.E, w.R, w.H, device=dev)
+            x = torch.from_numpy(d["x"].view(np.int16)).to(dev)
+            idx = torch.from_numpy(d["topk_idx"]).to(dev)
+            wt = torch.from_numpy(d["topk_w"]).to(dev)
+            b.dispatch(x, idx)
+            b.expert(mode)
+            b.combine(idx, wt)
+            torch.cuda.synchronize()
+            if int(b.status.item()) != 0:
+                raise RuntimeError(f"T={T}: device status {int(b.status.item())}")
+            row = {"T": T, "tokens": w.N * T,
+                   "fused_us": mean_us(capture(lambda: (b.dispatch(x, idx),
+                                                        b.combine(idx, wt))))}
+            if T <= args.sweep_ll_max:
+                llb = m.MoeLLBuffers(w.N, w.T, w.E, w.R, w.H, device=dev)
+                llb.dispatch(x, idx)
+                llb.expert(mode)
+                llb.combine(wt)
+                torch.cuda.synchronize()
+                if int(llb.status.item()) != 0 or not torch.equal(llb.out, b.out):
+                    raise RuntimeError(f"T={T}: low-latency output differs from the main path")
+                row["low_latency_us"] = mean_us(capture(lambda: (llb.dispatch(x, idx),
+                                                                 llb.combine(wt))))
+                del llb
+            rows.append(row)
+            del b
+            torch.cuda.empty_cache()
+    print(json.dumps({"sweep": "tokens per rank", "workload": args.config,
+                      "shape": {"N": base.N, "H": base.H, "E": base.E, "R": base.R},
+                      "steps": K, "warmup": W_, "timing": "CUDA-graph replay, L2 flushed "
+                      "before every step", "clocks": clk.summary(), "rows": rows}), flush=True)
+
+
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -964,8 +1045,17 @@ def main() -> None:
                     help="time the CPU oracle per configuration and phase, then exit")
     ap.add_argument("--profile-headline", action="store_true",
                     help="run only the headline step eight times without timing (for ncu)")
+    ap.add_argument("--token-sweep", action="store_true",
+                    help="time the layer against tokens per rank (fused and low-latency), "
+                         "then exit")
+    ap.add_argument("--sweep-tokens", type=int, nargs="+",
+                    default=[1, 4, 16, 32, 64, 128, 256, 512])
+    ap.add_argument("--sweep-ll-max", type=int, default=256,
+                    help="largest T of the sweep that also runs the low-latency calls")
     args = ap.parse_args()
-    if args.profile_headline:
+    if args.token_sweep:
+        token_sweep(args)
+    elif args.profile_headline:
         profile_headline(args)
     elif args.profile_pass:
         profile_pass(args)
