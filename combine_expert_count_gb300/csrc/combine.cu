@@ -22,11 +22,12 @@ namespace moe {
 // into fp32 accumulators with one fused multiply-add per slot in slot order
 // k = 0..R-1, rounding once to bf16 at the end.
 constexpr int kReduceGroup = 8;  // row loads kept in flight per chunk
-// Blocks per token in the fused combine, each a contiguous half of every
-// row, when a half still gives every thread at least one 16-byte chunk per
-// row (H >= 4096 with 256 threads): on the DSv3 EP16 combine two blocks per
-// token measured 84.6 us against 86.7 us with whole tokens (finer work evens
-// out the last wave of blocks); 4 or 8 were no better; on H = 2048 rows the
+// Fewest blocks per token in the fused combine (small batches take more,
+// see token_split): two, each a contiguous half of every row, when a half
+// still gives every thread at least one 16-byte chunk per row (H >= 4096
+// with 256 threads).  On the DSv3 EP16 combine two blocks per token
+// measured 84.6 us against 86.7 us with whole tokens (finer work evens out
+// the last wave of blocks); 4 or 8 were no better; on H = 2048 rows the
 // split would leave half of every block idle.
 static int combine_split(int H) { return (H >> 3) >= 2 * kGatherThreads ? 2 : 1; }
 
@@ -114,12 +115,8 @@ static cudaError_t reduce_grid(long long ntok, int H, int *split, int *grid) {
         return e;
     });
     if (err != cudaSuccess) return err;
-    long long sp = (long long)sm_count() * occ / ntok;
-    const long long most = (H >> 3) / kReduceThreads;
-    if (sp > most) sp = most;
-    if (sp < 1) sp = 1;
-    const long long nblk = ntok * sp;
-    *split = (int)sp;
+    *split = token_split(ntok, H, kReduceThreads, occ, 1);
+    const long long nblk = ntok * *split;
     *grid = (int)(nblk < (1LL << 30) ? nblk : (1LL << 30));
     return cudaSuccess;
 }
@@ -274,10 +271,21 @@ cudaError_t launch_combine_fused(const moe_shape &sh, int cap, const uint16_t *y
                                  uint16_t *csend, uint16_t *out, cudaStream_t st) {
     const long long ntok = (long long)sh.N * sh.T;
     if (ntok <= 0) return cudaSuccess;
-    const int split = combine_split(sh.H);
+    const int kr = sh.R <= 8 ? 8 : 0;
+    auto kern = kr ? k_combine_fused<8> : k_combine_fused<0>;
+    static LaunchMemo memo;
+    int occ = 1;
+    const cudaError_t err = memo.get(kr, &occ, [&](int *v) {
+        const cudaError_t e =
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(v, kern, kGatherThreads, 0);
+        if (*v < 1) *v = 1;
+        return e;
+    });
+    if (err != cudaSuccess) return err;
+    // small batches: more blocks per token, as for the reduce
+    const int split = token_split(ntok, sh.H, kGatherThreads, occ, combine_split(sh.H));
     const long long nblk = ntok * split;
     const int grid = (int)(nblk < (1LL << 30) ? nblk : (1LL << 30));
-    auto kern = sh.R <= 8 ? k_combine_fused<8> : k_combine_fused<0>;
     return launch_kernel(kern, dim3((unsigned)grid), dim3(kGatherThreads), 0, st, sh.N, sh.T, sh.E,
                          sh.R, sh.H, cap, split, y, idx, w, slot_row, eso, seg_off, send_off,
                          csend_off, csend, out);

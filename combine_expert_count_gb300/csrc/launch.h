@@ -111,6 +111,18 @@ cudaError_t launch_e4m3_encode(const float *v, uint8_t *out, int64_t n, cudaStre
 // SM count of the current device (cached per device).
 int sm_count();
 
+// Blocks per token for the kernels that give each token (or part of one) a
+// block: as many as a wave of resident blocks (SMs x `occ`) holds per token,
+// rounded down so that a batch filling the wave keeps one block per token,
+// at most one 16-byte chunk per thread of every row, and at least `least`.
+inline int token_split(long long ntok, int H, int threads, int occ, int least) {
+    long long sp = (long long)sm_count() * occ / (ntok > 0 ? ntok : 1);
+    const long long most = (H >> 3) / threads;
+    if (sp > most) sp = most;
+    if (sp < least) sp = least;
+    return (int)sp;
+}
+
 // A launch property of the current device (a kernel's occupancy, a cluster
 // limit) worked out by `fill` once per (device, key) and kept.  The lookup
 // and `fill` run under one lock: host threads calling at once neither race

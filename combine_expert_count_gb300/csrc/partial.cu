@@ -10,7 +10,8 @@
 // per assignment.  The receiver adds its token's partials in ascending rank
 // order in fp32 and rounds once more.
 //
-// One small block per token (grid-stride over tokens).  Warp 0 sorts the
+// One small block per token, or per part of a token's rows when the batch
+// is too small to fill the GPU (grid-stride over blocks).  Warp 0 sorts the
 // token's valid slots by (rank, slot) with one lane per slot, so each rank's
 // slots are consecutive and its last slot closes the partial; then every
 // thread takes 16-byte chunks of the row.
@@ -27,7 +28,8 @@ enum class PartialMode { kSend, kRecv, kFused };
 template <PartialMode kMode, int KR>  // KR > 0: R <= KR rows in registers; 0: any R
 __global__ void __launch_bounds__(kGatherThreads > kReduceThreads ? kGatherThreads
                                                                    : kReduceThreads)
-    k_combine_partial(int N, int T, int E, int R, int H, int cap, const uint16_t *__restrict__ y,
+    k_combine_partial(int N, int T, int E, int R, int H, int cap, int split,
+                      const uint16_t *__restrict__ y,
                       const int32_t *__restrict__ idx, const float *__restrict__ w,
                       const int32_t *__restrict__ slot_row, const int32_t *__restrict__ eso,
                       const int32_t *__restrict__ seg_off, uint16_t *__restrict__ pbuf,
@@ -43,7 +45,11 @@ __global__ void __launch_bounds__(kGatherThreads > kReduceThreads ? kGatherThrea
     __shared__ int nval;
     const int Er = E / N, cpr = H >> 3;
     const long long ntok = (long long)N * T;
-    for (long long tok = blockIdx.x; tok < ntok; tok += gridDim.x) {
+    // `split` blocks share a token, each a contiguous part of its rows
+    const int per = (cpr + split - 1) / split;
+    for (long long blk = blockIdx.x; blk < ntok * split; blk += gridDim.x) {
+        const long long tok = blk / split;
+        const int c0 = (int)(blk - tok * split) * per, c1 = min(cpr, c0 + per);
         const int s = (int)div_nonneg(tok, T);
         const int t = (int)(tok - (long long)s * T);
         if (threadIdx.x < 32) {
@@ -96,7 +102,7 @@ __global__ void __launch_bounds__(kGatherThreads > kReduceThreads ? kGatherThrea
                 ps[u] = on && oend[u] ? reinterpret_cast<uint4 *>(pbuf + op[u]) : nullptr;
                 wr[u] = on ? ow[u] : 0.0f;
             }
-            for (int c = threadIdx.x; c < cpr; c += blockDim.x) {
+            for (int c = c0 + threadIdx.x; c < c1; c += blockDim.x) {
                 float acc_o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
                 if constexpr (kReadY) {
                     uint4 v[KR];
@@ -129,7 +135,7 @@ __global__ void __launch_bounds__(kGatherThreads > kReduceThreads ? kGatherThrea
                 if (kWriteOut) orow[c] = pack_bf16x8(acc_o);
             }
         } else {
-            for (int c = threadIdx.x; c < cpr; c += blockDim.x) {
+            for (int c = c0 + threadIdx.x; c < c1; c += blockDim.x) {
                 float acc_o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
                 float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
                 for (int u = 0; u < nv; ++u) {
@@ -164,12 +170,24 @@ static cudaError_t launch_partial(const moe_shape &sh, int cap, const uint16_t *
                                   uint16_t *out, cudaStream_t st) {
     const long long ntok = (long long)sh.N * sh.T;
     if (ntok <= 0) return cudaSuccess;
-    const int grid = (int)(ntok < (1LL << 30) ? ntok : (1LL << 30));
-    auto kern = sh.R <= 8 ? k_combine_partial<kMode, 8> : k_combine_partial<kMode, 0>;
+    const int kr = sh.R <= 8 ? 8 : 0;
+    auto kern = kr ? k_combine_partial<kMode, 8> : k_combine_partial<kMode, 0>;
     // the receiving side only reads rows: the smaller block (see bf16.cuh)
     const int threads = kMode == PartialMode::kRecv ? kReduceThreads : kGatherThreads;
+    static LaunchMemo memo;
+    int occ = 1;
+    const cudaError_t err = memo.get(kr, &occ, [&](int *v) {
+        const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(v, kern, threads, 0);
+        if (*v < 1) *v = 1;
+        return e;
+    });
+    if (err != cudaSuccess) return err;
+    const int split = token_split(ntok, sh.H, threads, occ, 1);
+    const long long nblk = ntok * split;
+    const int grid = (int)(nblk < (1LL << 30) ? nblk : (1LL << 30));
     return launch_kernel(kern, dim3((unsigned)grid), dim3(threads), 0, st, sh.N, sh.T,
-                         sh.E, sh.R, sh.H, cap, y, idx, w, slot_row, eso, seg_off, pbuf, out);
+                         sh.E, sh.R, sh.H, cap, split, y, idx, w, slot_row, eso, seg_off, pbuf,
+                         out);
 }
 
 cudaError_t launch_combine_partial_send(const moe_shape &sh, int cap, const uint16_t *y,
