@@ -434,6 +434,24 @@ static bool is_host_memory(const void *p) {
     return a.type == cudaMemoryTypeHost;
 }
 
+// Piece length: whole rows up to kPieceElems; a batch with fewer pieces than
+// four per SM gets shorter ones (multiples of 128, at least MOE_MIN_PIECE
+// elements), so that its few tokens spread over more CTAs.
+#ifndef MOE_MIN_PIECE
+#define MOE_MIN_PIECE 1024
+#endif
+static_assert(MOE_MIN_PIECE % 128 == 0, "pieces hold whole scale blocks");
+static int piece_elems(long long ntok, int H) {
+    const int P = H < kPieceElems ? H : kPieceElems;
+    const long long want = (long long)sm_count() * 4;
+    if (ntok <= 0 || ntok * ((H + P - 1) / P) >= want) return P;
+    const long long per_tok = (want + ntok - 1) / ntok;
+    long long q = (H + per_tok - 1) / per_tok;
+    q = (q + 127) / 128 * 128;
+    if (q < MOE_MIN_PIECE) q = MOE_MIN_PIECE;
+    return q < P ? (int)q : P;
+}
+
 template <Dest kDest, bool kHostX>
 static cudaError_t launch_staged_x(const moe_shape &sh, const uint16_t *x,
                                    const int32_t *slot_row, uint8_t *send_q, float *send_s,
@@ -441,7 +459,7 @@ static cudaError_t launch_staged_x(const moe_shape &sh, const uint16_t *x,
                                    const LLDest &ll, cudaStream_t st) {
     const long long ntok = (long long)sh.N * sh.T;
     auto kern = k_quant_pack_staged<kDest, kHostX>;
-    const int P = sh.H < kPieceElems ? sh.H : kPieceElems;
+    const int P = piece_elems(ntok, sh.H);
     const long long nitems = ntok * ((sh.H + P - 1) / P);
     const int threads = quant_threads(P / 16);
     constexpr int kHist = kDest == Dest::kLowLatency ? MOE_MAX_EXPERTS * 4 : 0;
