@@ -52,8 +52,11 @@ __device__ __forceinline__ bool route_sender(int N, int T, int E, int R,
     __syncthreads();  // callers may reuse shared memory around this
 
     const int s = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nw = blockDim.x >> 5;
     const int TR = T * R, Er = E / N;
+    // warps that take ids (and own a table row): enough for 32 ids each, so a
+    // short batch clears and sums few rows (one token per rank on 256
+    // experts: the route took 8.9 us instead of 10.9 with all 32 warps)
+    const int nw = max(1, min((int)(blockDim.x >> 5), TR / 32 + (TR % 32 != 0)));
     const int32_t *id = idx + (size_t)s * TR;
     int32_t *srow = slot_row + (size_t)s * TR;
 
