@@ -529,7 +529,7 @@ static cudaError_t launch_signalled_x(const moe_shape &sh, int cap, const uint16
                                       int32_t *grp_src, int32_t *sig, int32_t *status,
                                       cudaStream_t st) {
     auto kern = k_dispatch_signalled<kHostX>;
-    const int P = sh.H < kPieceElems ? sh.H : kPieceElems;
+    const int P = piece_elems((long long)sh.N * sh.T, sh.H);
     const int npieces = (sh.H + P - 1) / P;
     const long long nitems = (long long)sh.N * sh.T * npieces;
     const int threads = quant_threads(P / 16);

@@ -37,7 +37,7 @@ def _workload(T, H):
     return base.replace(T=T, H=H, seed=base.seed + 500 + 7 * T + H)
 
 
-@pytest.mark.parametrize("calls", ["fused", "separate", "fused_route"])
+@pytest.mark.parametrize("calls", ["fused", "separate", "fused_route", "signalled"])
 @pytest.mark.parametrize("T,H", SHAPES)
 def test_main_path(T, H, calls):
     w = _workload(T, H)
