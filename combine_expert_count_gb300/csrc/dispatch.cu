@@ -29,11 +29,14 @@ __device__ __forceinline__ uint32_t cvt_pair(float a, float b) {
 // stores its 16 fp8 bytes straight from registers to the same place in each
 // of the token's R destination rows (one 512-byte coalesced store per warp
 // and row), the group's first thread also the scale.  Two x buffers let the
-// load of item n+1 overlap the arithmetic and stores of item n.  The fp8
-// rows are stored evict-first (st.global.cs): nothing reads them again
-// before a later call, and in the DSv3 EP16 layer (dispatch, then combine,
-// as one graph) the step took 137.6 us against 138.8 with default stores,
-// the dispatch itself unchanged.
+// load of item n+1 overlap the arithmetic and stores of item n.  The fused
+// and low-latency forms store their fp8 rows evict-first (st.global.cs):
+// nothing in the layer reads them again, and the DSv3 EP16 layer (dispatch,
+// then combine, as one graph) took 137.6 us against 138.8 with default
+// stores, the dispatch itself unchanged.  The send-only form keeps default
+// stores: its rows are read back next (by the receive pull, or by the
+// signalled kernel's own copy phase), which evict-first stores made 4 and
+// 1.2 us slower.
 //
 // Measured against staging the fp8 piece in shared memory and sending it
 // with R bulk (TMA) stores per destination: the direct stores are 2 us
@@ -296,7 +299,11 @@ __device__ __forceinline__ void quant_pack_body(
                 for (int k = 0; k < R; ++k) {
                     const long long row = rows[k];
                     if (row >= 0) {
-                        __stcs(reinterpret_cast<uint4 *>(send_q + row * H + off + c * 16), q);
+                        uint4 *d = reinterpret_cast<uint4 *>(send_q + row * H + off + c * 16);
+                        if constexpr (kDest == Dest::kSend)
+                            *d = q;  // read back soon after (receive pull, signalled copy)
+                        else
+                            __stcs(d, q);
                         if ((c & 7) == 0) send_s[row * Sb + sc] = scale;
                     }
                     if constexpr (kGrouped) {
