@@ -69,21 +69,34 @@ __device__ __forceinline__ bool route_sender(int N, int T, int E, int R,
     int *mytab = tab + warp * E;
     const unsigned lt = (1u << lane) - 1u;
     int bad = 0;
-    for (int r0 = lo; r0 < hi; r0 += 32) {
-        const int i = r0 + lane;
-        const int e = i < hi ? __ldg(id + i) : -1;
-        const bool good = (unsigned)e < (unsigned)E;
-        if (i < hi && !good) bad = 1;
-        const unsigned peers = __match_any_sync(kFull, good ? e : -1);
-        const int leader = __ffs(peers) - 1;
-        int before = 0;
-        if (good && lane == leader) {
-            before = mytab[e];
-            mytab[e] = before + __popc(peers);
+    // up to kAhead rounds of 32 ids are loaded before any is ranked, so a
+    // long share waits on one memory round trip per kAhead rounds, not per round
+    constexpr int kAhead = 8;
+    for (int r0 = lo; r0 < hi; r0 += 32 * kAhead) {
+        int ev[kAhead];
+#pragma unroll
+        for (int u = 0; u < kAhead; ++u) {
+            const int i = r0 + u * 32 + lane;
+            ev[u] = i < hi ? __ldg(id + i) : -1;
         }
-        before = __shfl_sync(kFull, before, leader);
-        if (i < hi) srow[i] = good ? before + __popc(peers & lt) : -1;
-        __syncwarp();
+#pragma unroll
+        for (int u = 0; u < kAhead; ++u) {
+            if (r0 + u * 32 >= hi) break;  // the same for the whole warp
+            const int i = r0 + u * 32 + lane;
+            const int e = ev[u];
+            const bool good = (unsigned)e < (unsigned)E;
+            if (i < hi && !good) bad = 1;
+            const unsigned peers = __match_any_sync(kFull, good ? e : -1);
+            const int leader = __ffs(peers) - 1;
+            int before = 0;
+            if (good && lane == leader) {
+                before = mytab[e];
+                mytab[e] = before + __popc(peers);
+            }
+            before = __shfl_sync(kFull, before, leader);
+            if (i < hi) srow[i] = good ? before + __popc(peers & lt) : -1;
+            __syncwarp();
+        }
     }
     const bool any_bad = __syncthreads_or(bad) != 0;
 
@@ -107,12 +120,26 @@ __device__ __forceinline__ bool route_sender(int N, int T, int E, int R,
     for (int p = tid; p <= N; p += blockDim.x)
         send_off[(size_t)s * (N + 1) + p] = p < N ? base[p * Er] : total;
 
-    // 3. slots (each lane revisits the ids it ranked in pass 1)
-    for (int r0 = lo; r0 < hi; r0 += 32) {
-        const int i = r0 + lane;
-        if (i < hi) {
-            const int e = __ldg(id + i);
-            if ((unsigned)e < (unsigned)E) srow[i] = base[e] + tab[warp * E + e] + srow[i];
+    // 3. slots (each lane revisits the ids it ranked in pass 1, kAhead rounds
+    // of ids and ranks loaded at a time)
+    for (int r0 = lo; r0 < hi; r0 += 32 * kAhead) {
+        int ev[kAhead], rv[kAhead];
+#pragma unroll
+        for (int u = 0; u < kAhead; ++u) {
+            const int i = r0 + u * 32 + lane;
+            ev[u] = -1;
+            rv[u] = 0;
+            if (i < hi) {
+                ev[u] = __ldg(id + i);
+                rv[u] = srow[i];  // this lane's own pass-1 store
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kAhead; ++u) {
+            const int i = r0 + u * 32 + lane;
+            const int e = ev[u];
+            if (i < hi && (unsigned)e < (unsigned)E)
+                srow[i] = base[e] + tab[warp * E + e] + rv[u];
         }
     }
     return any_bad;
