@@ -26,8 +26,7 @@
  *     - "Evaluation: dispatch/combine latency": block-scaled fp8 dispatch,
  *       bf16 combine.
  *
- * Readings where the pages leave a step open (each also listed in the
- * design notes):
+ * Readings where the pages leave a step open:
  *   - one row per (token, expert) assignment, no per-rank de-duplication;
  *   - expert e lives on rank e / (E/N) (contiguous blocks of E/N experts);
  *   - within one expert, rows keep ascending flattened index t*R + k;

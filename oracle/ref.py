@@ -6,8 +6,7 @@ from the CUDA package.  Arrays are numpy, bf16 values are uint16 bit patterns.
 
 Every function below marshals numpy arrays into one C function of the oracle;
 the arithmetic is all in ``moe_ref.c``.  Parity status of each function (what
-pins it to something other than itself) is listed in ``tests/test_oracle.py``
-and in the design notes.
+pins it to something other than itself) is listed in ``tests/test_oracle.py``.
 """
 from __future__ import annotations
 

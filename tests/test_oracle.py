@@ -21,8 +21,18 @@ What pins each oracle function:
                      brute-force positions (grp_src, tagged combine rows) on
                      every routing of tiny shapes; round trip through the
                      identity expert with weights summing to 1.
-  ref_weighted_sum   exact rational sum: result within one bf16 step.
+  ref_weighted_sum   exact rational sum: result within one bf16 step; every
+                     element equal, bit for bit, to a chain of fused
+                     multiply-adds in ascending slot order rounded by an
+                     exact-fraction fp32 rounder; hand cases where descending
+                     or pairwise order, or a separate multiply and add, give
+                     other bits.
   ref_standin_row    exact product in fractions, rounded by torch's bf16 cast.
+  ref_expert_standin / ref_standin_ll (per-expert scale)
+                     every grouped and low-latency row equals the stand-in of
+                     the expert its brute-force position says it belongs to
+                     (expert id from topk_idx), computed with numpy products
+                     and torch's bf16 cast.
   ref_combine_partial_send / _recv (send-side reduction)
                      exact rational sums on every routing of a tiny shape
                      and on random shapes with duplicates, bad ids and drops;
@@ -447,6 +457,134 @@ def test_weighted_sum_exact_within_one_bf16_step():
     assert _f32(ref.weighted_sum(rows, np.array([0.5, 0.5], np.float32)))[0] == 1.0
     assert _f32(ref.weighted_sum(rows, np.array([0.5, 0.5], np.float32),
                                  np.array([1, 0], np.int32)))[0] == 0.5
+
+
+def _rn32(v: Fraction) -> Fraction:
+    """v rounded to the nearest fp32 value, ties to even (normal and subnormal
+    ranges; no overflow in these cases), in exact fractions."""
+    if v == 0:
+        return Fraction(0)
+    a = abs(v)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    e = max(e, -126)                      # 2^e <= a < 2^(e+1), or the subnormal quantum
+    ulp = Fraction(2) ** (e - 23)
+    n, rest = divmod(a, ulp)
+    n = int(n)
+    if rest > ulp / 2 or (rest == ulp / 2 and n % 2 == 1):
+        n += 1
+    return (n * ulp) if v > 0 else -(n * ulp)
+
+
+def _fma_chain(w, y, order, fused=True) -> float:
+    """acc = 0; for k in order: acc = rn32(w_k * y_k + acc) (one rounding per
+    slot), or with fused=False rn32(rn32(w_k * y_k) + acc)."""
+    acc = Fraction(0)
+    for k in order:
+        p = Fraction(float(w[k])) * Fraction(float(y[k]))
+        acc = _rn32((p if fused else _rn32(p)) + acc)
+    return float(acc)
+
+
+def _bf16_of(v: float) -> int:
+    return int(torch.tensor([v], dtype=torch.float32).to(torch.bfloat16).view(torch.int16)
+               .item()) & 0xFFFF
+
+
+def test_weighted_sum_is_fma_chain_in_ascending_slot_order():
+    """Every output element is bf16_rn of the fp32 fused multiply-add chain
+    over the used slots in ascending order (the benchmark spec's fp32
+    accumulation in fixed top-k slot order), bit for bit."""
+    rng = np.random.default_rng(31)
+    for _ in range(60):
+        R, H = int(rng.integers(1, 9)), 16
+        rows = _bf16(rng.standard_normal((R, H)) * np.exp2(rng.integers(-6, 7, size=(R, 1))))
+        w = rng.dirichlet(np.ones(R)).astype(np.float32)
+        use = (rng.random(R) < 0.8).astype(np.int32)
+        got = ref.weighted_sum(rows, w, use)
+        y = _f32(rows).astype(np.float64)
+        order = [k for k in range(R) if use[k]]
+        for h in range(H):
+            assert int(got[h]) == _bf16_of(_fma_chain(w, y[:, h], order)), (R, h)
+
+
+def test_weighted_sum_order_hand_case():
+    """Rows 1, 2^-24, 2^-24, -1 with unit weights.  In ascending slot order
+    each 1 + 2^-24 is an fp32 tie that rounds to 1, so the result is 0;
+    descending order keeps both small terms (2^-23), and a pairwise tree
+    (1 + 2^-24) + (2^-24 - 1) keeps one (2^-24)."""
+    y = np.array([1.0, 2.0 ** -24, 2.0 ** -24, -1.0])
+    rows = _bf16(np.repeat(y[:, None], 4, axis=1))
+    w = np.ones(4, np.float32)
+    assert _fma_chain(w, y, [0, 1, 2, 3]) == 0.0
+    assert _fma_chain(w, y, [3, 2, 1, 0]) == 2.0 ** -23
+    pair = float(_rn32(_rn32(Fraction(1) + Fraction(2) ** -24) +
+                       _rn32(Fraction(2) ** -24 - 1)))
+    assert pair == 2.0 ** -24
+    assert np.all(_f32(ref.weighted_sum(rows, w)) == 0.0)
+
+
+def test_weighted_sum_fuses_multiply_and_add():
+    """Slot 0 gives -1, slot 1 adds w*y.  For seeded weights where rounding
+    the product to fp32 before the addition changes the bf16 result, the
+    oracle gives the fused result."""
+    rng = np.random.default_rng(77)
+    y = np.array([-1.0, 1.0 + 2.0 ** -7])
+    rows = _bf16(np.repeat(y[:, None], 2, axis=1))
+    hits = 0
+    for m in rng.integers(1, 2 ** 16, size=4000):
+        w = np.array([1.0, 1.0 + float(m) * 2.0 ** -23], np.float32)
+        fused, split = _fma_chain(w, y, [0, 1]), _fma_chain(w, y, [0, 1], fused=False)
+        if _bf16_of(fused) == _bf16_of(split):
+            continue
+        hits += 1
+        assert int(ref.weighted_sum(rows, w)[0]) == _bf16_of(fused)
+    assert hits >= 5
+
+
+def _standin_want(H, xrow, e, mode):
+    """The stand-in output of expert e for token row x: fp32 product of the
+    decoded code and its block scale (numpy, exact in float64 then one cast),
+    times s_e = 2^((e mod 3) - 1) (mode 1) or 1, rounded by torch's bf16 cast."""
+    q, sc = ref.quant_token(H, xrow)
+    dq = (ref.e4m3_decode(q) * np.repeat(sc.astype(np.float64), 128)).astype(np.float32)
+    se = np.float32(2.0 ** (e % 3 - 1)) if mode == 1 else np.float32(1.0)
+    return _bf16(dq * se)
+
+
+def _check_standin_lookup(N, T, E, R, H, idx, x, wt):
+    """Every grouped row (main layout) and every low-latency row holds the
+    stand-in of the expert that topk_idx names for it, found by brute force."""
+    Er = E // N
+    o = ref.layer(N, T, E, R, H, N * T * min(R, Er), x, idx, wt, mode=1)
+    ll = ref.layer_ll(N, T, E, R, H, x, idx, wt, mode=1)
+    _, grp, _ = brute.layouts(N, T, E, R, idx)
+    llr = brute.ll_rows(N, T, E, R, idx)
+    idx3 = np.asarray(idx).reshape(N, T, R)
+    for (s, t, k), g in grp.items():
+        e = int(idx3[s, t, k])
+        want = _standin_want(H, x[s, t], e, 1)
+        assert np.array_equal(o["y"][e // Er, g], want), (s, t, k)
+        assert np.array_equal(ll["y_ll"][llr[(s, t, k)]], want), (s, t, k)
+
+
+def test_standin_expert_lookup_mode1_all_routings_sampled():
+    rng = np.random.default_rng(41)
+    x = _tiny_x(2, 2, 128, 6)
+    allr = list(brute.all_routings(2, 2, 4, 2))
+    wt = np.full((2, 2, 2), 0.5, np.float32)
+    for i in rng.choice(len(allr), 120, replace=False):
+        _check_standin_lookup(2, 2, 4, 2, 128, allr[i], x, wt)
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen3_worst"])
+def test_standin_expert_lookup_mode1_configs(name):
+    w = W.CONFIGS[name]
+    if name == "qwen3_worst":
+        w = w.replace(T=4, H=256)
+    d = W.generate(w)
+    _check_standin_lookup(w.N, w.T, w.E, w.R, w.H, d["topk_idx"], d["x"], d["topk_w"])
 
 
 def test_standin_row_exact():
