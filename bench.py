@@ -266,38 +266,108 @@ def barrier(world: int) -> None:
 
 
 # ----------------------------------------------------------------- CPU oracle
+#
+# The CPU oracle as it stands, timed on the host cores over the same units
+# the GPU value times: route_count + exchange + dispatch_send +
+# dispatch_recv (dispatch) and combine_send + combine_recv (combine), on the
+# full workload (every token of every rank), the expert stand-in run once
+# outside the timer (oracle.ref.LayerTimer).
 
 
-def oracle_layer_us(w, sample_T: int, min_seconds: float, max_reps: int = 10):
-    """The CPU oracle, as it stands, on a sample of the workload (sample_T of
-    the T tokens per rank, all ranks); microseconds per full layer, scaled by
-    T / sample_T (every step is linear in the number of tokens)."""
-    from combine_expert_count_gb300 import workloads as W
+def oracle_layer_us(w, d, min_seconds: float, max_reps: int = 1000, warmup: int = 1):
+    """Single-threaded oracle: mean microseconds per full layer (dispatch,
+    combine, total) over whole layers until `min_seconds` of timed work (at
+    least one layer), and the number of layers timed."""
     from oracle import ref
-    ws = w.replace(T=sample_T, seed=w.seed + 17)
-    d = W.generate(ws)
-    mode = 1 if w.expert == "scale" else 0
-    times = []
-    t_start = time.perf_counter()
-    while len(times) < max_reps:
-        t0 = time.perf_counter()
-        rc = ref.route_count(ws.N, ws.T, ws.E, ws.R, d["topk_idx"])
-        ex = ref.exchange(ws.N, ws.E, 1 << 30, rc["expert_count"], rc["send_off"])
-        cap = max(1, int(ex["grp_off"][:, -1].max()))
-        ref.layer(ws.N, ws.T, ws.E, ws.R, ws.H, cap, d["x"], d["topk_idx"], d["topk_w"], mode)
-        times.append(time.perf_counter() - t0)
-        if time.perf_counter() - t_start >= min_seconds:
-            break
-    per_layer = statistics.median(times) * (w.T / sample_T) * 1e6
-    sample = (f"{ws.N} ranks x {sample_T} of {w.T} tokens/rank (H={w.H}, E={w.E}, top-{w.R}), "
-              f"{len(times)} runs, median, scaled x{w.T / sample_T:g}")
-    return per_layer, sample, sum(times)
+    lt = ref.LayerTimer(w.N, w.T, w.E, w.R, w.H, d["x"], d["topk_idx"], d["topk_w"],
+                        1 if w.expert == "scale" else 0)
+    for _ in range(warmup):
+        lt.step()
+    disp, comb = [], []
+    spent = 0.0
+    while len(disp) < max_reps and (not disp or spent < min_seconds):
+        a, b = lt.step()
+        disp.append(a)
+        comb.append(b)
+        spent += a + b
+    return (statistics.mean(disp) * 1e6, statistics.mean(comb) * 1e6,
+            statistics.mean(a + b for a, b in zip(disp, comb)) * 1e6, len(disp), spent)
+
+
+def _all_cores_worker(path, shape, mode, steps, barrier, queue):
+    """One process of the all-cores timing: its own copy of the layer."""
+    try:
+        from oracle import ref
+        z = np.load(path)
+        N, T, E, R, H = shape
+        lt = ref.LayerTimer(N, T, E, R, H, z["x"], z["topk_idx"], z["topk_w"], mode)
+        lt.step()                       # warm-up, untimed
+    except Exception as e:              # noqa: BLE001 -- reported to the parent
+        barrier.abort()
+        queue.put(repr(e))
+        return
+    barrier.wait()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        lt.step()
+    queue.put((t0, time.perf_counter()))
+
+
+def oracle_all_cores(w, d, steps: int = 2, procs: int = 0) -> dict:
+    """The oracle on every host core at once: `procs` processes (default one
+    per core), each timing `steps` full layers of the same workload after a
+    common start; microseconds per layer = wall time / layers finished.  The
+    oracle is plain single-threaded C, so the cores run independent layers
+    (throughput, not the latency of one layer)."""
+    import multiprocessing as mp
+    n = procs or os.cpu_count() or 1
+    ctx = mp.get_context("spawn")
+    with tempfile.TemporaryDirectory() as tmp:
+        path = os.path.join(tmp, "layer.npz")
+        np.savez(path, x=d["x"], topk_idx=d["topk_idx"], topk_w=d["topk_w"])
+        barrier, queue = ctx.Barrier(n), ctx.Queue()
+        ps = [ctx.Process(target=_all_cores_worker,
+                          args=(path, (w.N, w.T, w.E, w.R, w.H), 1 if w.expert == "scale" else 0,
+                                steps, barrier, queue)) for _ in range(n)]
+        for p in ps:
+            p.start()
+        spans = [queue.get(timeout=600) for _ in range(n)]
+        for p in ps:
+            p.join()
+    errors = [x for x in spans if isinstance(x, str)]
+    if errors:
+        raise RuntimeError(f"oracle all-cores worker failed: {errors[0]}")
+    wall = max(b for _, b in spans) - min(a for a, _ in spans)
+    return {"cores": n, "value": round(wall / (n * steps) * 1e6, 1), "unit": UNIT,
+            "layers": n * steps, "wall_s": round(wall, 2),
+            "how": f"{n} processes, each {steps} full layers after a common start; "
+                   "wall time / layers"}
+
+
+def cpu_baseline_line(w, d, min_seconds: float, all_cores: bool, warmup: int = 1,
+                      max_reps: int = 1000) -> dict:
+    import platform
+    dus, cus, tus, reps, spent = oracle_layer_us(w, d, min_seconds, max_reps, warmup)
+    line = {"value": round(tus, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"the full layer ({w.N} ranks x {w.T} tokens, H={w.H}, E={w.E}, "
+                      f"top-{w.R}), {reps} layers timed after {warmup} untimed, mean; "
+                      "route_count + exchange + dispatch_send + dispatch_recv + "
+                      "combine_send + combine_recv, stand-in outside the timer",
+            "dispatch_us": round(dus, 1), "combine_us": round(cus, 1),
+            "layers": reps, "cpu_seconds": round(spent, 2),
+            "cpu": platform.processor() or platform.machine(), "nproc": os.cpu_count()}
+    if all_cores:
+        line["all_cores"] = oracle_all_cores(w, d)
+    return line
 
 
 # ----------------------------------------------------------------- arms
 
 
 def run_reference(args) -> None:
+    """The reference arm: the CPU oracle as it stands, one full layer per
+    step on one host core (K timed layers after W untimed), plus the
+    all-cores figure; rank 0 only under torchrun."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -306,26 +376,23 @@ def run_reference(args) -> None:
     from oracle import ref
     ref.build()
     w = W.CONFIGS[args.config]
-    sample_T = max(1, min(w.T, args.ref_tokens))
-    for _ in range(args.warmup):
-        oracle_layer_us(w, sample_T, 0.0, max_reps=1)
-    vals = []
+    d = W.generate(w)
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        v, sample, _ = oracle_layer_us(w, sample_T, 0.0, max_reps=1)
-        vals.append(v)
+    cb = cpu_baseline_line(w, d, float("inf"), all_cores=not args.no_all_cores,
+                           warmup=args.warmup, max_reps=args.steps)
     wall = time.perf_counter() - t0
-    value = statistics.mean(vals)
+    value = cb["value"]
     line = {
-        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(value / 1000, 4), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "u8/f32 (plain C, fp32 accumulation)",
         "data": "synthetic (seeded)",
-        "config": {"workload": args.config, "N": w.N, "T": w.T, "H": w.H, "E": w.E, "R": w.R},
-        "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": sample},
-        "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
+        "config": {"workload": f"{args.config}: N={w.N} ranks x T={w.T} tokens, H={w.H}, "
+                               f"E={w.E}, top-{w.R}",
+                   "N": w.N, "T": w.T, "H": w.H, "E": w.E, "R": w.R},
+        "cpu_baseline": cb,
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "wall_s": round(wall, 1),
     }
@@ -409,73 +476,25 @@ def config_line(m, W, name, dev, capture, flush, K, W_) -> dict:
 def oracle_table(args) -> None:
     """The CPU oracle, as it stands, per configuration and phase (dispatch =
     route_count + exchange + dispatch_send + dispatch_recv; combine =
-    combine_send + combine_recv), single-threaded on a token sample scaled to
-    the full layer, and the whole layer on all host cores (one process per
-    core, each on its own sample); one JSON line."""
-    import multiprocessing as mp
+    combine_send + combine_recv), single-threaded on full layers, and the
+    DSv3 layer on all host cores; one JSON line."""
     import platform
     from combine_expert_count_gb300 import workloads as W
     from oracle import ref
     ref.build()
     out = {"cpu": platform.processor() or platform.machine(), "nproc": os.cpu_count(),
            "configs": []}
-    for name in ("tiny", "dsv3_decode", "kimi_k2_decode", "qwen3_skew", "prefill"):
+    for name in ("tiny", "dsv3_decode", "kimi_k2_decode", "qwen3_skew", "qwen3_worst", "prefill"):
         w = W.CONFIGS[name]
-        sample_T = min(w.T, 16 if w.T >= 16 else w.T)
-        ws = w.replace(T=sample_T, seed=w.seed + 17)
-        d = W.generate(ws)
-        t = oracle_phases(ws, d)
-        scale = w.T / sample_T
-        out["configs"].append({"workload": name, "sample_tokens_per_rank": sample_T,
-                               "dispatch_us": round(t[0] * scale * 1e6, 1),
-                               "combine_us": round(t[1] * scale * 1e6, 1)})
-    # all cores: one process per core, each timing a layer sample of dsv3_decode
-    n = os.cpu_count() or 1
-    ctx = mp.get_context("spawn")
-    with ctx.Pool(n) as pool:
-        pool.map(_oracle_worker, [0] * n)  # start-up and build, untimed
-        t0 = time.perf_counter()
-        per = pool.map(_oracle_worker, [1] * n)
-        wall = time.perf_counter() - t0
+        d = W.generate(w)
+        dus, cus, tus, reps, _ = oracle_layer_us(w, d, 0.0 if name == "prefill" else 3.0,
+                                                 max_reps=1 if name == "prefill" else 1000)
+        out["configs"].append({"workload": name, "layers": reps, "dispatch_us": round(dus, 1),
+                               "combine_us": round(cus, 1), "layer_us": round(tus, 1)})
+        del d
     w = W.CONFIGS["dsv3_decode"]
-    out["all_cores_dsv3_decode"] = {
-        "processes": n, "layers": n, "wall_s": round(wall, 3),
-        "us_per_layer": round(wall / n * (w.T / 16) * 1e6, 1),
-        "single_process_s_per_sample": round(statistics.median(per), 3),
-        "how": "n processes, each one 16-token-per-rank layer sample; wall / n, scaled x8"}
+    out["all_cores_dsv3_decode"] = oracle_all_cores(w, W.generate(w))
     print(json.dumps(out), flush=True)
-
-
-def oracle_phases(ws, d):
-    from oracle import ref
-    mode = 1 if ws.expert == "scale" else 0
-    t0 = time.perf_counter()
-    rc = ref.route_count(ws.N, ws.T, ws.E, ws.R, d["topk_idx"])
-    ex = ref.exchange(ws.N, ws.E, 1 << 30, rc["expert_count"], rc["send_off"])
-    cap = max(1, int(ex["grp_off"][:, -1].max()))  # exact fit: the oracle's buffers stay small
-    ds = ref.dispatch_send(ws.N, ws.T, ws.R, ws.H, d["x"], rc["slot_row"])
-    dr = ref.dispatch_recv(ws.N, ws.T, ws.E, ws.R, ws.H, cap, ds["send_q"], ds["send_s"],
-                           ds["send_tok"], rc["expert_count"], rc["expert_send_off"], ex["seg_off"])
-    t1 = time.perf_counter()
-    y = ref.expert_standin(ws.N, ws.E, ws.H, cap, mode, dr["grp_q"], dr["grp_s"], ex["grp_off"])
-    t2 = time.perf_counter()
-    cs = ref.combine_send(ws.N, ws.T, ws.E, ws.R, ws.H, cap, y, rc["expert_count"],
-                          rc["expert_send_off"], rc["send_off"], ex["seg_off"], ex["csend_off"])
-    ref.combine_recv(ws.N, ws.T, ws.E, ws.R, ws.H, cap, cs, d["topk_idx"], d["topk_w"],
-                     rc["slot_row"], rc["send_off"], ex["csend_off"])
-    t3 = time.perf_counter()
-    return t1 - t0, t3 - t2
-
-
-def _oracle_worker(timed: int) -> float:
-    from combine_expert_count_gb300 import workloads as W
-    w = W.CONFIGS["dsv3_decode"]
-    ws = w.replace(T=16, seed=w.seed + 17 + os.getpid() % 7)
-    d = W.generate(ws)
-    t0 = time.perf_counter()
-    if timed:
-        oracle_phases(ws, d)
-    return time.perf_counter() - t0
 
 
 def pairs_of(w, idx) -> int:
@@ -871,10 +890,8 @@ def run_ours(args) -> None:
         "wall_s_timed": round(t_wall, 3),
     }
     if world == 1 and not args.no_cpu_baseline:
-        v, sample, spent = oracle_layer_us(w, max(1, min(w.T, args.ref_tokens)), args.cpu_seconds,
-                                           max_reps=1000)
-        line["cpu_baseline"] = {"value": round(v, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
-                                "sample": sample, "cpu_seconds": round(spent, 1)}
+        line["cpu_baseline"] = cpu_baseline_line(w, d, args.cpu_seconds,
+                                                 all_cores=not args.no_all_cores)
     print(json.dumps(line), flush=True)
 
 
@@ -1032,10 +1049,10 @@ def main() -> None:
     ap.add_argument("--eager", action="store_true",
                     help="time eager launches instead of CUDA-graph replays")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--ref-tokens", type=int, default=16,
-                    help="tokens per rank in each oracle sample")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
-                    help="minimum CPU time spent on the oracle baseline")
+                    help="minimum CPU time spent on the single-threaded oracle baseline")
+    ap.add_argument("--no-all-cores", action="store_true",
+                    help="skip the oracle timing on every host core")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-skew", action="store_true",
                     help="skip the skewed-routing (Zipf) layer lines")

@@ -288,6 +288,75 @@ def layer(N, T, E, R, H, cap, x, topk_idx, topk_w, mode: int = 0) -> dict:
     return out
 
 
+class LayerTimer:
+    """The six steps of one layer timed on preallocated arrays, for the
+    benchmark's CPU baseline: route_count, exchange, dispatch_send and
+    dispatch_recv (the dispatch), combine_send and combine_recv (the
+    combine).  The routing and the expert stand-in run once when the timer is
+    built (the stand-in is not a timed step; its output is the same every
+    step, as on the GPU), the grouped buffers hold exactly the rows the
+    routing sends to the busiest rank, and no output array is allocated or
+    filled inside a timed step."""
+
+    def __init__(self, N, T, E, R, H, x, topk_idx, topk_w, mode: int = 0):
+        self.N, self.T, self.E, self.R, self.H = N, T, E, R, H
+        Er, Sb = E // N, H // 128
+        # private copies: the caller's arrays are never written
+        self.x = np.array(x, dtype=np.uint16, order="C").reshape(N, T, H)
+        self.idx = np.array(topk_idx, dtype=np.int32, order="C").reshape(N, T, R)
+        self.w = np.array(topk_w, dtype=np.float32, order="C").reshape(N, T, R)
+        inputs = (self.x, self.idx, self.w)
+        rc = route_count(N, T, E, R, self.idx)
+        ex = exchange(N, E, 1 << 30, rc["expert_count"], rc["send_off"])
+        self.cap = cap = max(1, int(ex["grp_off"][:, -1].max()))
+        z = np.zeros
+        self.cnt, self.send_off = z((N, E), np.int32), z((N, N + 1), np.int32)
+        self.eso, self.slot = z((N, E + 1), np.int32), z((N, T, R), np.int32)
+        self.grp_off, self.seg_off = z((N, Er + 1), np.int32), z((N, Er, N), np.int32)
+        self.csend_off, self.m_sizes = z((N, N + 1), np.int32), z((N, Er), np.int32)
+        self.send_q, self.send_s = z((N, T * R, H), np.uint8), z((N, T * R, Sb), np.float32)
+        self.send_tok = z((N, T * R), np.int32)
+        self.grp_q, self.grp_s = z((N, cap, H), np.uint8), z((N, cap, Sb), np.float32)
+        self.grp_src = z((N, cap, 2), np.int32)
+        self.csend, self.out = z((N, cap, H), np.uint16), z((N, T, H), np.uint16)
+        for a in vars(self).values():   # touch every output page once, outside any timed step
+            if isinstance(a, np.ndarray) and not any(a is i for i in inputs):
+                a.fill(0)
+        self.dispatch()
+        self.y = expert_standin(N, E, H, cap, mode, self.grp_q, self.grp_s, self.grp_off)
+
+    def dispatch(self) -> None:
+        L, N, T, E, R, H, cap = lib(), self.N, self.T, self.E, self.R, self.H, self.cap
+        L.ref_route_count(N, T, E, R, _i32(self.idx), _i32(self.cnt), _i32(self.send_off),
+                          _i32(self.eso), _i32(self.slot))
+        L.ref_exchange(N, E, cap, _i32(self.cnt), _i32(self.send_off), _i32(self.grp_off),
+                       _i32(self.seg_off), _i32(self.csend_off), _i32(self.m_sizes))
+        L.ref_dispatch_send(N, T, R, H, _u16(self.x), _i32(self.slot), _u8(self.send_q),
+                            _f32(self.send_s), _i32(self.send_tok))
+        L.ref_dispatch_recv(N, T, E, R, H, cap, _u8(self.send_q), _f32(self.send_s),
+                            _i32(self.send_tok), _i32(self.cnt), _i32(self.eso),
+                            _i32(self.seg_off), _u8(self.grp_q), _f32(self.grp_s),
+                            _i32(self.grp_src))
+
+    def combine(self) -> None:
+        L, N, T, E, R, H, cap = lib(), self.N, self.T, self.E, self.R, self.H, self.cap
+        L.ref_combine_send(N, T, E, R, H, cap, _u16(self.y), _i32(self.cnt), _i32(self.eso),
+                           _i32(self.send_off), _i32(self.seg_off), _i32(self.csend_off),
+                           _u16(self.csend))
+        L.ref_combine_recv(N, T, E, R, H, cap, _u16(self.csend), _i32(self.idx), _f32(self.w),
+                           _i32(self.slot), _i32(self.send_off), _i32(self.csend_off),
+                           _u16(self.out))
+
+    def step(self) -> tuple[float, float]:
+        """One layer; returns (dispatch seconds, combine seconds)."""
+        import time
+        t0 = time.perf_counter()
+        self.dispatch()
+        t1 = time.perf_counter()
+        self.combine()
+        return t1 - t0, time.perf_counter() - t1
+
+
 def layer_partial(N, T, E, R, H, cap, x, topk_idx, topk_w, mode: int = 0) -> dict:
     """``layer``, plus the combine with send-side reduction on the same expert
     outputs: ``part`` (partial rows) and ``out_partial``."""

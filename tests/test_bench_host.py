@@ -35,14 +35,19 @@ def test_algorithmic_bytes_match_formulas():
 def test_reference_arm_prints_one_json_line():
     env = dict(os.environ, WORLD_SIZE="1", RANK="0")
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
-                          "--config", "tiny", "--steps", "2", "--warmup", "1", "--ref-tokens", "4"],
+                          "--config", "tiny", "--steps", "2", "--warmup", "1"],
                          capture_output=True, text=True, env=env, timeout=300, check=True).stdout
     lines = [ln for ln in out.splitlines() if ln.startswith("{")]
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
     assert d["higher_is_better"] is False and d["value"] > 0
-    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] == 1
+    # every timed step is one whole layer (no extrapolation from a sample)
+    assert cb["layers"] == 2 and d["steps"] == 2
+    assert abs(cb["dispatch_us"] + cb["combine_us"] - d["value"]) <= 0.01 * d["value"] + 0.2
+    assert cb["all_cores"]["cores"] >= 1 and cb["all_cores"]["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0
 
 
