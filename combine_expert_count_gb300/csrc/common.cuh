@@ -114,6 +114,20 @@ __device__ __forceinline__ void st_release(int32_t *p, int v) {
     asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Address of `p` (this block's shared memory) in the shared memory of
+// cluster block `rank`, and a 32-bit load from such an address.
+__device__ __forceinline__ uint32_t dsmem_addr(const void *p, int rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ int ld_dsmem(uint32_t addr) {
+    int v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 // ------------------------------------------------------------ misc
 
 // Round a shared-memory pointer up to a 128-byte boundary.

@@ -36,7 +36,8 @@ cudaError_t launch_dispatch_fused(const moe_shape &sh, int cap, const uint16_t *
                                   const int32_t *idx, const int32_t *slot_row, const int32_t *eso,
                                   const int32_t *seg_off, uint8_t *send_q, float *send_s,
                                   int32_t *send_tok, uint8_t *grp_q, float *grp_s,
-                                  int32_t *grp_src, int32_t *status, cudaStream_t st);
+                                  int32_t *grp_src, int32_t *status, cudaStream_t st,
+                                  bool after_route = false);
 
 // Quantise + pack and the receive shuffle in one co-resident grid whose
 // CTAs hand rows over by per-(sender, receiver) arrival flags in `sig`

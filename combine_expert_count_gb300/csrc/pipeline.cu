@@ -25,6 +25,7 @@
 
 #include "launch.h"
 #include "moeroute.h"
+#include "trace.h"
 
 namespace {
 
@@ -53,6 +54,7 @@ static int check_dispatch(const moe_shape *sh, const moe_buffers *b, moe_sizes &
 }
 
 extern "C" int moe_dispatch_send_recv(const moe_shape *sh, const moe_buffers *b, void *stream) {
+    MOE_TRACE_CALL();
     moe_sizes z;
     int rc = check_dispatch(sh, b, z);
     if (rc != MOE_OK) return rc;
@@ -65,6 +67,7 @@ extern "C" int moe_dispatch_send_recv(const moe_shape *sh, const moe_buffers *b,
 }
 
 extern "C" int moe_dispatch(const moe_shape *sh, const moe_buffers *b, void *stream) {
+    MOE_TRACE_CALL();
     moe_sizes z;
     int rc = check_dispatch(sh, b, z);
     if (rc != MOE_OK) return rc;
@@ -73,11 +76,19 @@ extern "C" int moe_dispatch(const moe_shape *sh, const moe_buffers *b, void *str
                           b->m_sizes, b->status, reinterpret_cast<cudaStream_t>(stream)) !=
         cudaSuccess)
         return MOE_ECUDA;
-    return moe_dispatch_send_recv(sh, b, stream);
+    // the dispatch may start while the routing kernel runs (it waits for the
+    // routing outputs on the device)
+    if (moe::launch_dispatch_fused(*sh, (int)z.cap, b->x, b->topk_idx, b->slot_row,
+                                   b->expert_send_off, b->seg_off, b->send_q, b->send_s,
+                                   b->send_tok, b->grp_q, b->grp_s, b->grp_src, b->status,
+                                   reinterpret_cast<cudaStream_t>(stream), true) != cudaSuccess)
+        return MOE_ECUDA;
+    return MOE_OK;
 }
 
 extern "C" int moe_dispatch_signalled(const moe_shape *sh, const moe_buffers *b, int32_t *sig,
                                       void *stream) {
+    MOE_TRACE_CALL();
     moe_sizes z;
     int rc = check_dispatch(sh, b, z);
     if (rc != MOE_OK) return rc;
@@ -96,6 +107,7 @@ extern "C" int moe_dispatch_signalled(const moe_shape *sh, const moe_buffers *b,
 }
 
 extern "C" int moe_combine(const moe_shape *sh, const moe_buffers *b, void *stream) {
+    MOE_TRACE_CALL();
     moe_sizes z;
     int rc = moe_sizes_query(sh, &z);
     if (rc != MOE_OK) return rc;
@@ -116,6 +128,7 @@ extern "C" int moe_combine(const moe_shape *sh, const moe_buffers *b, void *stre
 
 extern "C" int moe_combine_partial(const moe_shape *sh, const moe_buffers *b, uint16_t *part,
                                    void *stream) {
+    MOE_TRACE_CALL();
     moe_sizes z;
     int rc = moe_sizes_query(sh, &z);
     if (rc != MOE_OK) return rc;

@@ -39,7 +39,12 @@ __device__ __forceinline__ void copy_rows(const Map &m, long long row0, long lon
     for (long long b = r0; b < r1; b += 32) {
         RowIdx d = {0, 0, 0};
         if (b + lane < r1) d = m.index(row0 + b + lane);
-        if constexpr (Map::kWaits) m.ready(d, deadline);
+        if constexpr (Map::kWaits) {
+            m.ready(d, deadline);
+            // lane q acquired row q's flag, but every lane reads row q: the
+            // warp barrier orders that acquire before the other lanes' loads
+            __syncwarp();
+        }
         if (d.kind == 1) m.side(d);
         const int cnt = (int)min(32LL, r1 - b);
         for (int q = 0; q < cnt; ++q) {

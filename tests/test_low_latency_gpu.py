@@ -99,11 +99,15 @@ def test_ll_output_equals_main_path():
 @pytest.mark.parametrize("N,T,E,R,H", [(1, 5, 4, 2, 128), (2, 16, 8, 3, 256), (3, 7, 6, 2, 384),
                                        (4, 33, 16, 4, 640), (2, 3, 4, 2, 8192 + 1024),
                                        (2, 9, 32, 12, 128), (2, 5, 64, 32, 256),
-                                       (2, 1024, 8, 2, 128), (4, 8, 1024, 32, 128)])
+                                       (2, 1024, 8, 2, 128), (4, 8, 1024, 32, 128),
+                                       (3, 700, 12, 4, 256), (2, 1024, 64, 32, 128),
+                                       (5, 520, 1000, 8, 128)])
 def test_ll_small_shapes(N, T, E, R, H):
     """Includes more than eight slots per token (the earlier-id count runs in
     groups of eight), 32 slots, the longest batch (T = 1024) and the most
-    experts (1024, the largest region-count histogram)."""
+    experts (1024, the largest region-count histogram); the last three have
+    more than 2048 ids per rank, so each sender's ids are ranked once in the
+    same launch (more experts than the CTA has threads in the last)."""
     w = W.Workload("llgrid", N=N, T=T, H=H, E=E, R=R, seed=N * 100 + T)
     d = W.generate(w)
     b = _run_ll(w, d, 0)
@@ -115,6 +119,21 @@ def test_ll_duplicates_overflow_and_bad_ids():
     d = W.generate(w)
     d["topk_idx"][0, :, :] = 1          # 12 rows for expert 1 from rank 0: 4 fit
     d["topk_idx"][1, 2, 1] = -3
+    b = _run_ll(w, d, 0)
+    o = ref.ll_rows(w.N, w.T, w.E, w.R, d["topk_idx"])
+    assert o["status"] == ref.ST_CAPACITY | ref.ST_BAD_EXPERT
+    _check_ll(w, d, b, 0)
+
+
+def test_ll_ranked_duplicates_overflow_and_bad_ids():
+    """The ranked form (more than 2048 ids per rank): regions that overflow
+    their T rows, duplicate experts inside a token and bad ids."""
+    w = W.Workload("llrank", N=2, T=600, H=256, E=4, R=4, seed=19)
+    d = W.generate(w)
+    d["topk_idx"][0, :, 0] = 1           # 600 rows of sender 0 for expert 1, plus duplicates
+    d["topk_idx"][0, :300, 1] = 1
+    d["topk_idx"][1, 7, 2] = -1
+    d["topk_idx"][1, 9, 3] = 4
     b = _run_ll(w, d, 0)
     o = ref.ll_rows(w.N, w.T, w.E, w.R, d["topk_idx"])
     assert o["status"] == ref.ST_CAPACITY | ref.ST_BAD_EXPERT
