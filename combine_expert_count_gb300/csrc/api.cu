@@ -9,6 +9,7 @@
 
 #include "launch.h"
 #include "moeroute.h"
+#include "trace.h"
 
 namespace moe {
 
@@ -133,6 +134,7 @@ static int check_ll(const moe_shape *sh, moe_sizes *z) {
 int moe_route_count(const moe_shape *sh, const int32_t *topk_idx, int32_t *expert_count,
                     int32_t *send_off, int32_t *expert_send_off, int32_t *slot_row,
                     int32_t *status, void *stream) {
+    MOE_TRACE_CALL();
     moe_sizes z;
     int rc = moe_sizes_query(sh, &z);
     if (rc != MOE_OK) return rc;
@@ -147,6 +149,7 @@ int moe_route_count(const moe_shape *sh, const int32_t *topk_idx, int32_t *exper
 int moe_exchange(const moe_shape *sh, const int32_t *expert_count, const int32_t *send_off,
                  int32_t *grp_off, int32_t *seg_off, int32_t *csend_off, int32_t *m_sizes,
                  int32_t *status, void *stream) {
+    MOE_TRACE_CALL();
     moe_sizes z;
     int rc = moe_sizes_query(sh, &z);
     if (rc != MOE_OK) return rc;
@@ -163,6 +166,7 @@ int moe_route(const moe_shape *sh, const int32_t *topk_idx, int32_t *expert_coun
               int32_t *send_off, int32_t *expert_send_off, int32_t *slot_row, int32_t *grp_off,
               int32_t *seg_off, int32_t *csend_off, int32_t *m_sizes, int32_t *status,
               void *stream) {
+    MOE_TRACE_CALL();
     moe_sizes z;
     int rc = moe_sizes_query(sh, &z);
     if (rc != MOE_OK) return rc;
@@ -180,6 +184,7 @@ int moe_route(const moe_shape *sh, const int32_t *topk_idx, int32_t *expert_coun
 int moe_dispatch_send(const moe_shape *sh, const uint16_t *x_bf16, const int32_t *slot_row,
                       uint8_t *send_q, float *send_s, int32_t *send_tok, int32_t *status,
                       void *stream) {
+    MOE_TRACE_CALL();
     moe_sizes z;
     int rc = moe_sizes_query(sh, &z);
     if (rc != MOE_OK) return rc;
@@ -195,6 +200,7 @@ int moe_dispatch_recv(const moe_shape *sh, const uint8_t *send_q, const float *s
                       const int32_t *send_tok, const int32_t *expert_count,
                       const int32_t *expert_send_off, const int32_t *seg_off, uint8_t *grp_q,
                       float *grp_s, int32_t *grp_src, int32_t *status, void *stream) {
+    MOE_TRACE_CALL();
     moe_sizes z;
     int rc = moe_sizes_query(sh, &z);
     if (rc != MOE_OK) return rc;
@@ -213,6 +219,7 @@ int moe_combine_send(const moe_shape *sh, const uint16_t *y_bf16, const int32_t 
                      const int32_t *expert_send_off, const int32_t *send_off,
                      const int32_t *seg_off, const int32_t *csend_off, uint16_t *csend,
                      int32_t *status, void *stream) {
+    MOE_TRACE_CALL();
     moe_sizes z;
     int rc = moe_sizes_query(sh, &z);
     if (rc != MOE_OK) return rc;
@@ -229,6 +236,7 @@ int moe_combine_recv(const moe_shape *sh, const uint16_t *csend, const int32_t *
                      const float *topk_w, const int32_t *slot_row, const int32_t *send_off,
                      const int32_t *csend_off, uint16_t *out_bf16, int32_t *status,
                      void *stream) {
+    MOE_TRACE_CALL();
     moe_sizes z;
     int rc = moe_sizes_query(sh, &z);
     if (rc != MOE_OK) return rc;
@@ -245,6 +253,7 @@ int moe_combine_partial_send(const moe_shape *sh, const uint16_t *y_bf16, const 
                              const float *topk_w, const int32_t *slot_row,
                              const int32_t *expert_send_off, const int32_t *seg_off,
                              uint16_t *part, void *stream) {
+    MOE_TRACE_CALL();
     moe_sizes z;
     int rc = moe_sizes_query(sh, &z);
     if (rc != MOE_OK) return rc;
@@ -260,6 +269,7 @@ int moe_combine_partial_send(const moe_shape *sh, const uint16_t *y_bf16, const 
 
 int moe_combine_partial_recv(const moe_shape *sh, const uint16_t *part, const int32_t *topk_idx,
                              const int32_t *slot_row, uint16_t *out_bf16, void *stream) {
+    MOE_TRACE_CALL();
     moe_sizes z;
     int rc = moe_sizes_query(sh, &z);
     if (rc != MOE_OK) return rc;
@@ -272,6 +282,7 @@ int moe_combine_partial_recv(const moe_shape *sh, const uint16_t *part, const in
 
 int moe_expert_standin(const moe_shape *sh, int mode, const uint8_t *grp_q, const float *grp_s,
                        const int32_t *grp_off, uint16_t *y_bf16, void *stream) {
+    MOE_TRACE_CALL();
     moe_sizes z;
     int rc = moe_sizes_query(sh, &z);
     if (rc != MOE_OK) return rc;
@@ -286,6 +297,7 @@ int moe_expert_standin(const moe_shape *sh, int mode, const uint8_t *grp_q, cons
 int moe_dispatch_ll(const moe_shape *sh, const uint16_t *x_bf16, const int32_t *topk_idx,
                     uint8_t *ll_q, float *ll_s, int32_t *ll_src, int32_t *ll_count,
                     int32_t *ll_row, int32_t *status, void *stream) {
+    MOE_TRACE_CALL();
     moe_sizes z;
     int rc = check_ll(sh, &z);
     if (rc != MOE_OK) return rc;
@@ -300,6 +312,7 @@ int moe_dispatch_ll(const moe_shape *sh, const uint16_t *x_bf16, const int32_t *
 
 int moe_expert_standin_ll(const moe_shape *sh, int mode, const uint8_t *ll_q, const float *ll_s,
                           const int32_t *ll_count, uint16_t *y_ll, void *stream) {
+    MOE_TRACE_CALL();
     moe_sizes z;
     int rc = check_ll(sh, &z);
     if (rc != MOE_OK) return rc;
@@ -313,6 +326,7 @@ int moe_expert_standin_ll(const moe_shape *sh, int mode, const uint8_t *ll_q, co
 
 int moe_combine_ll(const moe_shape *sh, const uint16_t *y_ll, const float *topk_w,
                    const int32_t *ll_row, uint16_t *out_bf16, int32_t *status, void *stream) {
+    MOE_TRACE_CALL();
     moe_sizes z;
     int rc = check_ll(sh, &z);
     if (rc != MOE_OK) return rc;
@@ -323,6 +337,7 @@ int moe_combine_ll(const moe_shape *sh, const uint16_t *y_ll, const float *topk_
 }
 
 int moe_e4m3_encode(const float *v, uint8_t *out, int64_t n, void *stream) {
+    MOE_TRACE_CALL();
     if (n < 0) return MOE_EINVAL;
     if (n > 0 && (v == nullptr || out == nullptr)) return MOE_EINVAL;
     return cuda_rc(moe::launch_e4m3_encode(v, out, n, as_stream(stream)));

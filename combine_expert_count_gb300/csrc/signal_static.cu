@@ -22,6 +22,7 @@
 #include <cuda_runtime.h>
 
 #include "moeroute.h"
+#include "trace.h"
 
 namespace {
 
@@ -59,6 +60,7 @@ int scratch_ptr(int32_t **out) {
 
 extern "C" int moe_dispatch_signalled_static(const moe_shape *sh, const moe_buffers *b,
                                              void *stream) {
+    MOE_TRACE_CALL();
     moe_sizes z;
     int rc = moe_sizes_query(sh, &z);
     if (rc != MOE_OK) return rc;
