@@ -103,6 +103,24 @@ def test_pinned_host_x_and_out(calls):
     assert int(buf.status.item()) == 0
 
 
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["prefill", "qwen3_worst"])
+def test_config_full_size_every_element(name):
+    """The two largest workloads at their configured sizes (prefill: 8 ranks
+    x 4096 tokens; the worst case: 16 ranks x 512 tokens all routed to rank
+    0's experts, the receive bound of the EFA page's "Send and receive
+    buffers"), in the launch the benchmark times (default capacity), every
+    output element against the oracle, compared rank by rank."""
+    w = W.CONFIGS[name]
+    d = W.generate(w)
+    buf = G.run_path(w, G.to_dev(d))
+    o = _oracle(w, d, _exact_cap(w, d))
+    G.compare_with_oracle_by_rank(w, buf, o)
+    if name == "qwen3_worst":
+        recv = G.host(buf.grp_off)[:, -1]
+        assert recv[0] == w.N * w.T * min(w.R, w.Er) and np.all(recv[1:] == 0)
+
+
 def test_worst_case_reduced_t_full_parity():
     """All tokens routed to rank 0's experts, compared in full."""
     w = W.CONFIGS["qwen3_worst"].replace(T=64)
