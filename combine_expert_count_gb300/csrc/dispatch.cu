@@ -51,9 +51,47 @@ __device__ __forceinline__ uint32_t cvt_pair(float a, float b) {
 constexpr int kPieceElems = MOE_PIECE_ELEMS;
 static_assert(kPieceElems % 128 == 0, "pieces hold whole scale blocks");
 
-// Shared memory of the staged body for piece size P: two bf16 x buffers;
-// the low-latency histogram follows.
-__host__ __device__ constexpr size_t stage_bytes(int P) { return (size_t)4 * P; }
+// x buffers of the staged body: the load of item n + kNB - 1 is issued when
+// item n starts, so a CTA keeps up to kNB - 1 pieces in flight (kNB when it
+// prefetches before a gate).  The pack into the send buffer (and, fused, the
+// grouped layout) uses MOE_PACK_STAGES buffers; its pieces are whole rows
+// (up to kPieceElems) for batches of more than MOE_PACK_LONG tokens per
+// resident CTA, else rows halved to at most MOE_PACK_PIECE elements (more,
+// smaller items for short batches, and five CTAs per SM instead of three).
+// The low-latency forms and the signalled dispatch, which spend per-item
+// work on finding or publishing rows, use two buffers of whole rows.
+// Measured on the layer graphs against two whole-row buffers: DSv3 EP16
+// (2.7 tokens per CTA) 136.5 us with four half-row buffers, 138.9 with four
+// whole-row ones, 136.5 with two; Kimi-K2 EP32 (5.4 tokens per CTA) 259.4,
+// 257.5, 261.1; prefill EP8 (43 tokens per CTA) 1975, 1933, 1977; the
+// low-latency dispatch took 40.4 against 35.9 us with half rows (its
+// per-item search runs twice per token).
+#ifndef MOE_PACK_STAGES
+#define MOE_PACK_STAGES 4
+#endif
+#ifndef MOE_PACK_PIECE
+#define MOE_PACK_PIECE 4096
+#endif
+#ifndef MOE_PACK_LONG
+#define MOE_PACK_LONG 4
+#endif
+static_assert(MOE_PACK_STAGES >= 2 && MOE_PACK_STAGES <= 8, "two to eight x buffers");
+static_assert(MOE_PACK_PIECE % 128 == 0, "pieces hold whole scale blocks");
+
+// Buffers and largest piece of each form of the staged body.
+enum class Dest { kSend, kSendGrouped, kLowLatency, kLowLatencyRanked };
+__host__ __device__ constexpr int x_stages(Dest d, bool signal) {
+    return (d == Dest::kSend || d == Dest::kSendGrouped) && !signal ? MOE_PACK_STAGES : 2;
+}
+__host__ __device__ constexpr int piece_cap(Dest d, bool signal, bool long_batch = false) {
+    return (d == Dest::kSend || d == Dest::kSendGrouped) && !signal && !long_batch
+               ? MOE_PACK_PIECE
+               : kPieceElems;
+}
+
+// Shared memory of the staged body for piece size P and kNB buffers: the
+// bf16 x buffers; the low-latency histogram or counting tables follow.
+__host__ __device__ constexpr size_t stage_bytes(int P, int nb) { return (size_t)nb * 2 * P; }
 
 __device__ __forceinline__ uint4 quant16(const uint4 &a, const uint4 &b, float scale) {
     const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
@@ -77,10 +115,10 @@ __device__ __forceinline__ float amax16(const uint4 &a, const uint4 &b) {
     return m;
 }
 
-// Where the quantised rows go: the send buffer (moe_dispatch_send), the send
-// buffer and the grouped layout (fused dispatch), or the low-latency layout
-// (rows found per token by the CTA, or ranked per sender first: kLowLatencyRanked).
-enum class Dest { kSend, kSendGrouped, kLowLatency, kLowLatencyRanked };
+// Where the quantised rows go (Dest above): the send buffer
+// (moe_dispatch_send), the send buffer and the grouped layout (fused
+// dispatch), or the low-latency layout (rows found per token by the CTA, or
+// ranked per sender first: kLowLatencyRanked).
 
 // Low-latency layout: receiver r keeps a T-row region per (local expert j,
 // sender s); assignment (t, k) of s with expert e = r*Er + j takes row
@@ -171,8 +209,9 @@ __device__ __forceinline__ void publish_row(const Signal &sg, int g, int target)
 // are issued: the barrier that ends the item orders every thread's stores
 // before the publishing thread's release fence.
 // The CTA handles items cta, cta + ncta, ...
+// Returns the number of items the CTA processed, or -1 after a timeout.
 template <Dest kDest, bool kHostX, bool kSignal = false, class Gate = NoGate>
-__device__ __forceinline__ void quant_pack_body(
+__device__ __forceinline__ int quant_pack_body(
     int T, int R, int H, int P, long long tok0, long long nitems, const uint16_t *__restrict__ x,
     const int32_t *__restrict__ slot_row, uint8_t *__restrict__ send_q, float *__restrict__ send_s,
     int32_t *__restrict__ send_tok, int32_t *__restrict__ status, const GroupedDest &gd,
@@ -180,22 +219,22 @@ __device__ __forceinline__ void quant_pack_body(
     constexpr bool kGrouped = kDest == Dest::kSendGrouped;
     constexpr bool kLL = kDest == Dest::kLowLatency;
     constexpr bool kLLR = kDest == Dest::kLowLatencyRanked;
+    constexpr int kXStages = x_stages(kDest, kSignal);
     extern __shared__ __align__(128) unsigned char smem_raw[];
     unsigned char *sm = align128(smem_raw);
     uint16_t *xbuf = reinterpret_cast<uint16_t *>(sm);  // [2][P] bf16
-    __shared__ uint64_t xbar[2];
+    __shared__ uint64_t xbar[kXStages];
     __shared__ long long rows[MOE_MAX_TOPK];   // destination rows of the current item
     __shared__ long long grows[MOE_MAX_TOPK];  // and its grouped rows (kGrouped)
     __shared__ int wpart[8][MOE_MAX_TOPK];  // LL: per-warp counts of earlier equal ids
-    int *hist = reinterpret_cast<int *>(sm + stage_bytes(P));  // [E], LL
+    int *hist = reinterpret_cast<int *>(sm + stage_bytes(P, kXStages));  // [E], LL
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthr = blockDim.x;
     const int Sb = H >> 7, npieces = (H + P - 1) / P;
     const long long TR = (long long)T * R;
 
     if (tid == 0) {
-        mbar_init(&xbar[0], 1);
-        mbar_init(&xbar[1], 1);
+        for (int b = 0; b < kXStages; ++b) mbar_init(&xbar[b], 1);
         fence_mbar_init();
     }
     __syncthreads();
@@ -209,13 +248,13 @@ __device__ __forceinline__ void quant_pack_body(
     };
 
     const long long first = cta, G = ncta;
-    if (!kHostX && tid == 0 && first < nitems) issue_load(first, 0);
-    if constexpr (Gate::kPrefetch) {
-        // both buffers' pieces of x before the gate, past which everything
-        // that another kernel or phase writes is read
-        if (!kHostX && tid == 0 && first + G < nitems) issue_load(first + G, 1);
-        gate(reinterpret_cast<int *>(sm + stage_bytes(P)));
-    }
+    // the first kXStages - 1 pieces; with a gate every buffer's piece before
+    // it, past which everything that another kernel or phase writes is read
+    constexpr int kPre = Gate::kPrefetch ? kXStages : kXStages - 1;
+    if (!kHostX && tid == 0)
+        for (int i = 0; i < kPre && first + (long long)i * G < nitems; ++i)
+            issue_load(first + (long long)i * G, i);
+    if constexpr (Gate::kPrefetch) gate(reinterpret_cast<int *>(sm + stage_bytes(P, kXStages)));
     bool timed_out = false;
     // thread tid < R: destinations of the current item, read one item ahead
     long long prow = -1, pgrow = -1;
@@ -230,16 +269,20 @@ __device__ __forceinline__ void quant_pack_body(
     };
     if (!kLL && tid < R && first < nitems) next_rows(first);
 
-    int n = 0;
-    for (long long item = first; item < nitems; item += G, ++n) {
-        const int b = n & 1;
+    int n = 0, b = 0;   // item count, its buffer (n mod kXStages)
+    uint32_t par = 0;   // phase parity of buffer b's barrier: (n / kXStages) & 1
+    for (long long item = first; item < nitems;
+         item += G, ++n, b = (b + 1 == kXStages) ? 0 : b + 1, par ^= (b == 0) ? 1u : 0u) {
         const long long tok = tok0 + div_nonneg(item, npieces);
         const int piece = (int)(item - (tok - tok0) * npieces);
         const int off = piece * P, len = min(P, H - off), nch = len >> 4;
         const long long s = div_nonneg(tok, T);
         const int t = (int)(tok - s * T);
-        if (!kHostX && tid == 0 && item + G < nitems && !(Gate::kPrefetch && n == 0))
-            issue_load(item + G, b ^ 1);
+        // the piece kXStages - 1 items ahead, into the buffer the previous
+        // item released (already issued before the gate when n == 0)
+        const long long ahead = item + (long long)(kXStages - 1) * G;
+        if (!kHostX && tid == 0 && ahead < nitems && !(Gate::kPrefetch && n == 0))
+            issue_load(ahead, b == 0 ? kXStages - 1 : b - 1);
         if constexpr (kLL) {
             // rows of this token in the low-latency layout, while x arrives:
             // u_k = earlier assignments of rank s with the same expert, eight
@@ -306,7 +349,7 @@ __device__ __forceinline__ void quant_pack_body(
             for (int i = tid; i < (len >> 3); i += nthr) dst[i] = src[i];
             __syncthreads();
         } else {
-            const bool ok = mbar_wait(&xbar[b], (uint32_t)((n >> 1) & 1));
+            const bool ok = mbar_wait(&xbar[b], par);
             if (__syncthreads_or(!ok)) {
                 timed_out = true;
                 break;
@@ -375,11 +418,13 @@ __device__ __forceinline__ void quant_pack_body(
     }
     if (tid == 0 && timed_out) {
         flag(status, MOE_ST_TIMEOUT);
-        // let the loads of items n and n+1 land before shared memory goes away
-        mbar_wait(&xbar[n & 1], (uint32_t)((n >> 1) & 1));
-        if (first + (long long)(n + 1) * G < nitems)
-            mbar_wait(&xbar[(n + 1) & 1], (uint32_t)(((n + 1) >> 1) & 1));
+        // let every issued load (items n .. n + kXStages - 1) land before
+        // shared memory goes away
+        for (int i = n; i < n + kXStages; ++i)
+            if (first + (long long)i * G < nitems)
+                mbar_wait(&xbar[i % kXStages], (uint32_t)((i / kXStages) & 1));
     }
+    return timed_out ? -1 : n;
 }
 
 // kPdl: launched as the programmatic dependent of the routing kernel (the
@@ -387,8 +432,14 @@ __device__ __forceinline__ void quant_pack_body(
 // griddepcontrol.wait, so the first pieces arrive while the routing kernel
 // runs; nothing the routing kernel writes is read, and nothing is written,
 // before the wait.
+// At most MOE_QUANT_MAXNREG registers per thread, so that five 224-thread
+// CTAs (a 7168-element row in 3584-element pieces, 16 elements a thread,
+// or whole rows in two passes) fit on an SM.
+#ifndef MOE_QUANT_MAXNREG
+#define MOE_QUANT_MAXNREG 56
+#endif
 template <Dest kDest, bool kHostX, bool kPdl = false>
-__global__ void __launch_bounds__(256)
+__global__ void __maxnreg__(MOE_QUANT_MAXNREG)
     k_quant_pack_staged(int T, int R, int H, int P, long long tok0, long long nitems,
                         const uint16_t *__restrict__ x, const int32_t *__restrict__ slot_row,
                         uint8_t *__restrict__ send_q, float *__restrict__ send_s,
@@ -447,7 +498,7 @@ struct LLRankGate {
 };
 
 #ifndef MOE_LL_RANKED_MINB
-#define MOE_LL_RANKED_MINB 1
+#define MOE_LL_RANKED_MINB 4
 #endif
 template <bool kHostX>
 __global__ void __launch_bounds__(256, MOE_LL_RANKED_MINB)
@@ -553,15 +604,17 @@ static bool is_host_memory(const void *p) {
     return a.type == cudaMemoryTypeHost;
 }
 
-// Piece length: whole rows up to kPieceElems; a batch with fewer pieces than
-// four per SM gets shorter ones (multiples of 128, at least MOE_MIN_PIECE
-// elements), so that its few tokens spread over more CTAs.
+// Piece length: rows split into the fewest pieces of at most `cap`
+// elements, of equal length (multiples of 128); a batch with fewer pieces
+// than four per SM gets shorter ones (at least MOE_MIN_PIECE elements), so
+// that its few tokens spread over more CTAs.
 #ifndef MOE_MIN_PIECE
 #define MOE_MIN_PIECE 1024
 #endif
 static_assert(MOE_MIN_PIECE % 128 == 0, "pieces hold whole scale blocks");
-static int piece_elems(long long ntok, int H) {
-    const int P = H < kPieceElems ? H : kPieceElems;
+static int piece_elems(long long ntok, int H, int cap) {
+    const int np = (H + cap - 1) / cap;
+    const int P = ((H + np - 1) / np + 127) / 128 * 128;
     const long long want = (long long)sm_count() * 4;
     if (ntok <= 0 || ntok * ((H + P - 1) / P) >= want) return P;
     const long long per_tok = (want + ntok - 1) / ntok;
@@ -578,17 +631,21 @@ static cudaError_t launch_staged_x(const moe_shape &sh, const uint16_t *x,
                                    const LLDest &ll, cudaStream_t st) {
     const long long ntok = (long long)sh.N * sh.T;
     auto kern = k_quant_pack_staged<kDest, kHostX, kPdl>;
-    const int P = piece_elems(ntok, sh.H);
+    constexpr int kNB = x_stages(kDest, false);
+    // a long batch: more than MOE_PACK_LONG tokens per CTA of five per SM
+    const bool long_batch = ntok > (long long)MOE_PACK_LONG * 5 * sm_count();
+    const int cap = piece_cap(kDest, false, long_batch);
+    const int P = piece_elems(ntok, sh.H, cap);
     const long long nitems = ntok * ((sh.H + P - 1) / P);
     const int threads = quant_threads(P / 16);
     constexpr int kHist = kDest == Dest::kLowLatency ? MOE_MAX_EXPERTS * 4 : 0;
-    const int smem = (int)stage_bytes(P) + 128 + kHist;
+    const int smem = (int)stage_bytes(P, kNB) + 128 + kHist;
     static LaunchMemo memo;
     int occ = 1;
     cudaError_t err = memo.get(((long long)smem << 16) | threads, &occ, [&](int *v) {
         // the attribute allows the largest piece, whatever this call's P
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)stage_bytes(kPieceElems) + 128 + kHist);
+                                             (int)stage_bytes(kPieceElems, kNB) + 128 + kHist);
         if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(v, kern, threads, smem);
         if (*v < 1) *v = 1;
         return e;
@@ -640,18 +697,19 @@ static cudaError_t launch_ll_ranked_x(const moe_shape &sh, const uint16_t *x, ui
                                       const LLDest &ll, cudaStream_t st) {
     const long long ntok = (long long)sh.N * sh.T;
     auto kern = k_dispatch_ll_ranked<kHostX>;
-    const int P = piece_elems(ntok, sh.H);
+    constexpr int kNB = x_stages(Dest::kLowLatencyRanked, false);
+    const int P = piece_elems(ntok, sh.H, piece_cap(Dest::kLowLatencyRanked, false));
     const long long nitems = ntok * ((sh.H + P - 1) / P);
     const int threads = quant_threads(P / 16);
     // x buffers, then the counting tables of one sender: [E+1] + [warps][E] ints
     const auto tables = [](int E, int thr) { return (size_t)(E + 1 + (thr / 32) * E) * 4; };
-    const int smem = (int)(stage_bytes(P) + 128 + tables(sh.E, threads));
+    const int smem = (int)(stage_bytes(P, kNB) + 128 + tables(sh.E, threads));
     static LaunchMemo memo;
     int occ = 0;
     cudaError_t err = memo.get(((long long)smem << 16) | threads, &occ, [&](int *v) {
         cudaError_t e = cudaFuncSetAttribute(
             kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-            (int)(stage_bytes(kPieceElems) + 128 + tables(MOE_MAX_EXPERTS, 256)));
+            (int)(stage_bytes(kPieceElems, kNB) + 128 + tables(MOE_MAX_EXPERTS, 256)));
         if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(v, kern, threads, smem);
         return e;
     });
@@ -705,16 +763,17 @@ static cudaError_t launch_signalled_x(const moe_shape &sh, int cap, const uint16
                                       int32_t *grp_src, int32_t *sig, int32_t *status,
                                       cudaStream_t st) {
     auto kern = k_dispatch_signalled<kHostX>;
-    const int P = piece_elems((long long)sh.N * sh.T, sh.H);
+    constexpr int kNB = x_stages(Dest::kSend, true);
+    const int P = piece_elems((long long)sh.N * sh.T, sh.H, piece_cap(Dest::kSend, true));
     const int npieces = (sh.H + P - 1) / P;
     const long long nitems = (long long)sh.N * sh.T * npieces;
     const int threads = quant_threads(P / 16);
-    const int smem = (int)stage_bytes(P) + 128;
+    const int smem = (int)stage_bytes(P, kNB) + 128;
     static LaunchMemo memo;
     int occ = 1;
     cudaError_t err = memo.get(((long long)smem << 16) | threads, &occ, [&](int *v) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)stage_bytes(kPieceElems) + 128);
+                                             (int)stage_bytes(kPieceElems, kNB) + 128);
         if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(v, kern, threads, smem);
         if (*v < 1) *v = 1;
         return e;
