@@ -95,15 +95,15 @@ def measured_peak():
 # Source files each kernel is built from: its DRAM-traffic record holds only
 # while these are unchanged.
 KERNEL_SOURCES = {
-    "route": ("route.cu", "common.cuh"),
-    "dispatch_fused": ("dispatch.cu", "shuffle.cuh", "common.cuh"),
+    "route": ("route.cu", "rank.cuh", "common.cuh"),
+    "dispatch_fused": ("dispatch.cu", "rank.cuh", "shuffle.cuh", "common.cuh"),
     "combine_fused": ("combine.cu", "bf16.cuh", "common.cuh"),
-    "dispatch_send": ("dispatch.cu", "shuffle.cuh", "common.cuh"),
+    "dispatch_send": ("dispatch.cu", "rank.cuh", "shuffle.cuh", "common.cuh"),
     "dispatch_recv": ("shuffle.cu", "shuffle.cuh", "common.cuh"),
     "combine_send": ("shuffle.cu", "shuffle.cuh", "common.cuh"),
     "combine_recv": ("combine.cu", "bf16.cuh", "common.cuh"),
     "combine_partial": ("partial.cu", "bf16.cuh", "common.cuh"),
-    "dispatch_signalled": ("dispatch.cu", "shuffle.cuh", "common.cuh"),
+    "dispatch_signalled": ("dispatch.cu", "rank.cuh", "shuffle.cuh", "common.cuh"),
 }
 
 
@@ -428,9 +428,55 @@ def per_kernel_table(nbytes, favg, savg, rcx_k, A, w, workload) -> list:
     return rows
 
 
-def config_line(m, W, name, dev, capture, flush, K, W_) -> dict:
-    """Fused and separate-call layer times on another configuration, against
-    the 70%-of-nominal target of the separate calls' algorithmic bytes."""
+def fused_split(m, b, idx, wt, x, flush, K, peak) -> dict:
+    """Eager per-kernel times of the fused calls on one workload (L2 flushed
+    before each step; an event after each launch): the route (latency-bound),
+    the fused dispatch and the fused combine, each with its algorithmic
+    bytes, GB/s and fraction of the measured copy peak."""
+    import torch
+    sh = b.shape
+    tens = b.tensors(x=x, topk_idx=idx, topk_w=wt)
+    calls = (lambda: m.moe_route(sh, idx, b.expert_count, b.send_off, b.expert_send_off,
+                                 b.slot_row, b.grp_off, b.seg_off, b.csend_off, b.m_sizes,
+                                 b.status),
+             lambda: m.moe_dispatch_send_recv(sh, tens), lambda: m.moe_combine(sh, tens))
+    st = torch.cuda.current_stream()
+    for _ in range(3):
+        flush.zero_()
+        for c in calls:
+            c()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    for k in range(K):
+        flush.zero_()
+        evs[k][0].record(st)
+        for i, c in enumerate(calls):
+            c()
+            evs[k][i + 1].record(st)
+    torch.cuda.synchronize()
+    us = [statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs) * 1000 for i in range(3)]
+    A = int(b.send_off[:, -1].sum().item())
+    w = types_ns(N=b.N, T=b.T, H=b.H, R=b.R)
+    nb = algorithmic_bytes(w, A)["fused"]
+    out = {"route_us": round(us[0], 2)}
+    for name, u in (("dispatch_fused", us[1]), ("combine_fused", us[2])):
+        gbs = nb[name] / (u * 1e-6) / 1e9
+        out[name] = {"us": round(u, 2), "algorithmic_mb": round(nb[name] / 1e6, 1),
+                     "algorithmic_gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)}
+    out["dispatch_us"] = round(us[0] + us[1], 2)
+    out["combine_us"] = round(us[2], 2)
+    return out
+
+
+def types_ns(**kw):
+    import types
+    return types.SimpleNamespace(**kw)
+
+
+def config_line(m, W, name, dev, capture, flush, K, W_, peak) -> dict:
+    """Another configuration: fused and separate-call layer times (CUDA-graph
+    replay), the dispatch / combine split with each fused kernel's roofline
+    fraction (eager launches), and the 70%-of-nominal target of the
+    separate-call byte model."""
     import torch
     w = W.CONFIGS[name]
     d = W.generate(w)
@@ -465,8 +511,11 @@ def config_line(m, W, name, dev, capture, flush, K, W_) -> dict:
         res[key] = round(statistics.mean(a.elapsed_time(c) for a, c in tt) * 1000, 2)
     moved = sum(nb["fused"].values())
     s8d = nb["s8d_dispatch"] + nb["s8d_combine"]
+    res["bytes_moved_mb"] = round(moved / 1e6, 1)
     res["achieved_gbs"] = round(moved / (res["us"] * 1e-6) / 1e9, 1)
-    res["algorithmic_mb_s8d"] = round(s8d / 1e6, 1)
+    res["frac_of_peak"] = round(moved / (res["us"] * 1e-6) / 1e9 / peak, 4)
+    res.update(fused_split(m, b, idx, wt, x, flush, K, peak))
+    res["separate_call_model_mb"] = round(s8d / 1e6, 1)
     res["target_us_70pct_nominal"] = round(s8d / (0.7 * NOMINAL_HBM_GBS * 1e9) * 1e6, 1)
     del b
     torch.cuda.empty_cache()
@@ -530,7 +579,7 @@ def partial_combine_line(m, buf, w, d, x, idx, wt, tens, capture, time_steps, ti
                    "CUDA-graph replay; combine_kernel_us alone"}
 
 
-def skew_line(m, W, name, dev, capture, flush, K, W_) -> dict:
+def skew_line(m, W, name, dev, capture, flush, K, W_, peak) -> dict:
     """One layer (moe_dispatch + moe_combine, and with moe_combine_partial) on
     a skewed-routing workload."""
     import torch
@@ -566,6 +615,7 @@ def skew_line(m, W, name, dev, capture, flush, K, W_) -> dict:
         res[key] = round(statistics.mean(a.elapsed_time(c) for a, c in tt) * 1000, 2)
     res["rows_sent_send_side"] = pairs_of(w, d["topk_idx"])
     res["rows_sent_receive_side"] = int(b.send_off[:, -1].sum().item())
+    res.update(fused_split(m, b, idx, wt, x, flush, K, peak))
     del b
     torch.cuda.empty_cache()
     return res
@@ -812,10 +862,10 @@ def run_ours(args) -> None:
                                    time_kernels, flush, K, W_, world)
     others = None
     if rank == 0 and not args.no_skew:
-        others = [config_line(m, W, name, dev, capture, flush, min(K, 20), W_)
+        others = [config_line(m, W, name, dev, capture, flush, min(K, 20), W_, measured_peak()[0])
                   for name in ("kimi_k2_decode", "prefill")]
     if rank == 0 and not args.no_skew:
-        skew = [skew_line(m, W, name, dev, capture, flush, K, W_)
+        skew = [skew_line(m, W, name, dev, capture, flush, K, W_, measured_peak()[0])
                 for name in ("qwen3_zipf0", "qwen3_zipf0.5", "qwen3_zipf1", "qwen3_zipf1.5",
                              "qwen3_skew")]
     else:
@@ -835,7 +885,6 @@ def run_ours(args) -> None:
     peak, peak_kind = measured_peak()
     us = mean_step_ms * 1000
     moved = sum(nbytes["fused"].values())
-    s8d = nbytes["s8d_dispatch"] + nbytes["s8d_combine"]
     achieved = moved / (us * 1e-6) / 1e9
     favg = {n: statistics.mean(v) for n, v in zip(FUSED, fused_k)}
     savg = {n: statistics.mean(v) for n, v in zip(KERNELS, sep_k)}
@@ -869,9 +918,12 @@ def run_ours(args) -> None:
         "frac_of_peak": round(achieved / peak, 4), "peak_gbs": peak, "peak_kind": peak_kind,
         "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
         "bytes_moved_mb": {k: round(v / 1e6, 1) for k, v in nbytes["fused"].items()},
-        "algorithmic_mb_s8d": {"dispatch": round(nbytes["s8d_dispatch"] / 1e6, 1),
-                               "combine": round(nbytes["s8d_combine"] / 1e6, 1)},
-        "effective_gbs_s8d": round(s8d / (us * 1e-6) / 1e9, 1),
+        "separate_call_model_mb": {"dispatch": round(nbytes["s8d_dispatch"] / 1e6, 1),
+                                   "combine": round(nbytes["s8d_combine"] / 1e6, 1),
+                                   "note": "bytes if every buffer of the six separate calls is "
+                                           "written once and read once; the fused calls skip "
+                                           "two of those reads, so no bandwidth is quoted on "
+                                           "this model"},
         "kernel_us": {n: round(v * 1000, 2) for n, v in favg.items()},
         "separate_kernel_us": {n: round(v * 1000, 2) for n, v in savg.items()},
         "roofline": {"bound": "hbm", "kernel": KERNEL_SYMBOL[dom],
@@ -955,6 +1007,77 @@ def profile_headline(args) -> None:
     if int(buf.status.item()) != 0:
         raise RuntimeError(f"device status {int(buf.status.item())}")
     print("headline profile pass done: 8 steps of 3 library launches", flush=True)
+
+
+PROFILE_CALLS = ("route", "dispatch", "combine", "dispatch_send", "dispatch_recv",
+                 "combine_send", "combine_recv", "dispatch_ll", "combine_ll", "signalled",
+                 "partial")
+
+
+def profile_kernel(args) -> None:
+    """One call form launched a few times for a single-kernel ncu capture,
+    nothing timed: one untimed pass of the whole layer (which launches every
+    kernel of the path once), then `--profile-reps` launches of the named call,
+    L2 flushed before each.  With --cap (grouped rows per rank) or --tokens
+    the case stays small enough for a full-set capture."""
+    import torch
+
+    from combine_expert_count_gb300 import moeroute as m
+    from combine_expert_count_gb300 import workloads as W
+
+    w = W.CONFIGS[args.config]
+    if args.tokens:
+        w = w.replace(T=args.tokens)
+    d = W.generate(w)
+    dev = torch.device("cuda", 0)
+    buf = m.MoeBuffers(w.N, w.T, w.E, w.R, w.H, cap=args.cap, device=dev)
+    x = torch.from_numpy(d["x"].view(np.int16)).to(dev)
+    idx = torch.from_numpy(d["topk_idx"]).to(dev)
+    wt = torch.from_numpy(d["topk_w"]).to(dev)
+    mode = 1 if w.expert == "scale" else 0
+    sh = buf.shape
+    tens = buf.tensors(x=x, topk_idx=idx, topk_w=wt)
+    buf.dispatch(x, idx)
+    buf.expert(mode)
+    buf.combine(idx, wt)
+    ll = None
+    if args.profile_kernel in ("dispatch_ll", "combine_ll"):
+        ll = m.MoeLLBuffers(w.N, w.T, w.E, w.R, w.H, device=dev)
+        ll.dispatch(x, idx)
+        ll.expert(mode)
+        ll.combine(wt)
+    calls = {
+        "route": lambda: buf.route(idx),
+        "dispatch": lambda: m.moe_dispatch_send_recv(sh, tens),
+        "combine": lambda: m.moe_combine(sh, tens),
+        "dispatch_send": lambda: m.moe_dispatch_send(sh, x, buf.slot_row, buf.send_q, buf.send_s,
+                                                     buf.send_tok, buf.status),
+        "dispatch_recv": lambda: m.moe_dispatch_recv(sh, buf.send_q, buf.send_s, buf.send_tok,
+                                                     buf.expert_count, buf.expert_send_off,
+                                                     buf.seg_off, buf.grp_q, buf.grp_s,
+                                                     buf.grp_src, buf.status),
+        "combine_send": lambda: m.moe_combine_send(sh, buf.y, buf.expert_count,
+                                                   buf.expert_send_off, buf.send_off, buf.seg_off,
+                                                   buf.csend_off, buf.csend, buf.status),
+        "combine_recv": lambda: m.moe_combine_recv(sh, buf.csend, idx, wt, buf.slot_row,
+                                                   buf.send_off, buf.csend_off, buf.out,
+                                                   buf.status),
+        "dispatch_ll": lambda: ll.dispatch(x, idx),
+        "combine_ll": lambda: ll.combine(wt),
+        "signalled": lambda: buf.dispatch(x, idx, calls="signalled"),
+        "partial": lambda: buf.combine(idx, wt, calls="partial"),
+    }
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(args.profile_reps):
+        flush.zero_()
+        calls[args.profile_kernel]()
+    torch.cuda.synchronize()
+    st = int(buf.status.item())
+    if st != 0:
+        raise RuntimeError(f"device status {st}")
+    print(f"profile-kernel {args.profile_kernel}: {args.config} N={w.N} T={w.T} H={w.H} E={w.E} "
+          f"top-{w.R} cap={buf.cap}, {args.profile_reps} launches after one layer pass, "
+          f"{buf.device_bytes() / 1e9:.2f} GB of buffers", flush=True)
 
 
 def token_sweep(args) -> None:
@@ -1062,6 +1185,12 @@ def main() -> None:
                     help="time the CPU oracle per configuration and phase, then exit")
     ap.add_argument("--profile-headline", action="store_true",
                     help="run only the headline step eight times without timing (for ncu)")
+    ap.add_argument("--profile-kernel", choices=PROFILE_CALLS,
+                    help="launch one call a few times without timing (for a single-kernel "
+                         "ncu capture), then exit")
+    ap.add_argument("--profile-reps", type=int, default=3)
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="tokens per rank for --profile-kernel (0: the config's)")
     ap.add_argument("--token-sweep", action="store_true",
                     help="time the layer against tokens per rank (fused and low-latency), "
                          "then exit")
@@ -1070,7 +1199,9 @@ def main() -> None:
     ap.add_argument("--sweep-ll-max", type=int, default=256,
                     help="largest T of the sweep that also runs the low-latency calls")
     args = ap.parse_args()
-    if args.token_sweep:
+    if args.profile_kernel:
+        profile_kernel(args)
+    elif args.token_sweep:
         token_sweep(args)
     elif args.profile_headline:
         profile_headline(args)
