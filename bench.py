@@ -428,7 +428,7 @@ def per_kernel_table(nbytes, favg, savg, rcx_k, A, w, workload) -> list:
     return rows
 
 
-def fused_split(m, b, idx, wt, x, flush, K, peak) -> dict:
+def fused_split(m, b, idx, wt, x, flush, K, peak, workload=None) -> dict:
     """Eager per-kernel times of the fused calls on one workload (L2 flushed
     before each step; an event after each launch): the route (latency-bound),
     the fused dispatch and the fused combine, each with its algorithmic
@@ -462,6 +462,9 @@ def fused_split(m, b, idx, wt, x, flush, K, peak) -> dict:
         gbs = nb[name] / (u * 1e-6) / 1e9
         out[name] = {"us": round(u, 2), "algorithmic_mb": round(nb[name] / 1e6, 1),
                      "algorithmic_gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)}
+        dram = dram_traffic(name, workload) if workload else None
+        if dram is not None:
+            out[name]["dram_mb_ncu"] = round(dram / 1e6, 1)
     out["dispatch_us"] = round(us[0] + us[1], 2)
     out["combine_us"] = round(us[2], 2)
     return out
@@ -514,7 +517,7 @@ def config_line(m, W, name, dev, capture, flush, K, W_, peak) -> dict:
     res["bytes_moved_mb"] = round(moved / 1e6, 1)
     res["achieved_gbs"] = round(moved / (res["us"] * 1e-6) / 1e9, 1)
     res["frac_of_peak"] = round(moved / (res["us"] * 1e-6) / 1e9 / peak, 4)
-    res.update(fused_split(m, b, idx, wt, x, flush, K, peak))
+    res.update(fused_split(m, b, idx, wt, x, flush, K, peak, name))
     res["separate_call_model_mb"] = round(s8d / 1e6, 1)
     res["target_us_70pct_nominal"] = round(s8d / (0.7 * NOMINAL_HBM_GBS * 1e9) * 1e6, 1)
     del b
@@ -615,7 +618,7 @@ def skew_line(m, W, name, dev, capture, flush, K, W_, peak) -> dict:
         res[key] = round(statistics.mean(a.elapsed_time(c) for a, c in tt) * 1000, 2)
     res["rows_sent_send_side"] = pairs_of(w, d["topk_idx"])
     res["rows_sent_receive_side"] = int(b.send_off[:, -1].sum().item())
-    res.update(fused_split(m, b, idx, wt, x, flush, K, peak))
+    res.update(fused_split(m, b, idx, wt, x, flush, K, peak, name))
     del b
     torch.cuda.empty_cache()
     return res
