@@ -1002,14 +1002,21 @@ def profile_headline(args) -> None:
     buf.dispatch(x, idx)
     buf.expert(1 if w.expert == "scale" else 0)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    xin, out = x, None
+    if args.host_io:
+        # the end-to-end form: x read from and out written to pinned host memory
+        xin = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+        xin.copy_(x)
+        out = torch.empty(buf.out.shape, dtype=buf.out.dtype, pin_memory=True)
     for _ in range(8):
         flush.zero_()
-        buf.dispatch(x, idx)
-        buf.combine(idx, wt)
+        buf.dispatch(xin, idx)
+        buf.combine(idx, wt, out=out)
     torch.cuda.synchronize()
     if int(buf.status.item()) != 0:
         raise RuntimeError(f"device status {int(buf.status.item())}")
-    print("headline profile pass done: 8 steps of 3 library launches", flush=True)
+    print("headline profile pass done: 8 steps of 3 library launches"
+          + (" (pinned host x and out)" if args.host_io else ""), flush=True)
 
 
 PROFILE_CALLS = ("route", "dispatch", "combine", "dispatch_send", "dispatch_recv",
@@ -1188,6 +1195,9 @@ def main() -> None:
                     help="time the CPU oracle per configuration and phase, then exit")
     ap.add_argument("--profile-headline", action="store_true",
                     help="run only the headline step eight times without timing (for ncu)")
+    ap.add_argument("--host-io", action="store_true",
+                    help="with --profile-headline: x and out in pinned host memory (the "
+                         "end-to-end form)")
     ap.add_argument("--profile-kernel", choices=PROFILE_CALLS,
                     help="launch one call a few times without timing (for a single-kernel "
                          "ncu capture), then exit")
