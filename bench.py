@@ -14,7 +14,9 @@ the timed window.
 Prints one JSON line: value = dispatch + combine microseconds per layer
 (lower is better), achieved HBM GB/s over the bytes the timed calls must
 move, the roofline of the dominant kernel, an end-to-end figure with host
-buffers, and the CPU oracle timed on a bounded sample as a baseline.
+buffers, the other configurations with their dispatch / combine split, and
+the CPU oracle (whole layers of the same steps, one core and all cores) as
+a baseline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
   python bench.py --impl reference ...   (the CPU oracle as the reference arm)

@@ -494,8 +494,10 @@ def _bf16_of(v: float) -> int:
 
 def test_weighted_sum_is_fma_chain_in_ascending_slot_order():
     """Every output element is bf16_rn of the fp32 fused multiply-add chain
-    over the used slots in ascending order (the benchmark spec's fp32
-    accumulation in fixed top-k slot order), bit for bit."""
+    over the used slots in ascending order (fp32 accumulation in a fixed
+    top-k slot order of the weighted average the combine takes: "Enabling
+    trillion-parameter models on AWS EFA", "Dispatch and combine"), bit for
+    bit."""
     rng = np.random.default_rng(31)
     for _ in range(60):
         R, H = int(rng.integers(1, 9)), 16
