@@ -743,6 +743,11 @@ def run_ours(args) -> None:
         return [a.elapsed_time(b) for a, b in evs]
 
     def time_kernels(calls, n):
+        # untimed passes of the same eager sequence first: the first eager
+        # launches after the graph replays measured several µs slow
+        for _ in range(W_):
+            flush.zero_()
+            run_calls(calls)
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
                for _ in range(n)]
         for k in range(n):
