@@ -294,7 +294,11 @@ int moe_dispatch_send_recv(const moe_shape *shape, const moe_buffers *b, void *s
 /* moe_route, then moe_dispatch_send_recv.  Uses x,
  * topk_idx, the routing arrays, the send buffers and the grouped buffers;
  * *status is cleared first.  Outputs: everything moe_route_count,
- * moe_exchange, moe_dispatch_send and moe_dispatch_recv write. */
+ * moe_exchange, moe_dispatch_send and moe_dispatch_recv write.  The
+ * dispatch kernel is launched as the routing kernel's programmatic
+ * dependent: it starts loading x while the routing kernel runs and waits on
+ * the device for its outputs (x must therefore be complete when the call is
+ * made, as for every other call; the stream order before the call is kept). */
 int moe_dispatch(const moe_shape *shape, const moe_buffers *b, void *stream);
 
 /* moe_combine_send + moe_combine_recv in one kernel.  Uses y, topk_idx,
@@ -412,7 +416,10 @@ int moe_dispatch_signalled_static(const moe_shape *shape, const moe_buffers *b, 
 
 /* Quantise every token (as moe_dispatch_send) and place its rows, scales and
  * token id in the low-latency layout; writes ll_row and ll_count.  Clears
- * *status first; MOE_ST_BAD_EXPERT / MOE_ST_CAPACITY as for the main path. */
+ * *status first; MOE_ST_BAD_EXPERT / MOE_ST_CAPACITY as for the main path.
+ * One kernel: with at most 2048 ids per rank each token's rows come from a
+ * count of the sender's earlier ids; longer batches rank every sender's ids
+ * once in the same (co-resident) launch first.  The outputs are the same. */
 int moe_dispatch_ll(const moe_shape *shape, const uint16_t *x_bf16, const int32_t *topk_idx,
                     uint8_t *ll_q, float *ll_s, int32_t *ll_src, int32_t *ll_count,
                     int32_t *ll_row, int32_t *status, void *stream);
