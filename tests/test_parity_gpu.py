@@ -353,3 +353,48 @@ def test_limits(N, T, E, R, H, calls):
     d = W.generate(w)
     G.compare_with_oracle(w, G.run_path(w, G.to_dev(d), calls=calls),
                           _oracle(w, d, w.default_cap))
+
+
+def test_dispatch_reads_x_written_just_before():
+    """moe_dispatch's quantiser starts loading x while its routing kernel runs
+    (programmatic dependent launch). x written by a kernel issued just
+    before the call on the same stream, eagerly and inside a CUDA graph, must
+    still be the x it reads: the grouped rows match the oracle on the new x."""
+    w = W.CONFIGS["dsv3_decode"].replace(T=32)
+    d_a = W.generate(w)
+    d_b = W.generate(w.replace(seed=w.seed + 99))
+    dd_a, dd_b = G.to_dev(d_a), G.to_dev(d_b)
+    x = dd_a["x"].clone()
+    buf = m.MoeBuffers(w.N, w.T, w.E, w.R, w.H)
+    idx = dd_a["topk_idx"]
+    o_b = ref.layer(w.N, w.T, w.E, w.R, w.H, buf.cap, d_b["x"], d_a["topk_idx"], d_a["topk_w"],
+                    mode=1)
+    recv = o_b["grp_off"][:, -1]
+
+    def check():
+        torch.cuda.synchronize()
+        gq, sq = G.host(buf.grp_q), G.host(buf.send_q)
+        for r in range(w.N):
+            G.assert_eq(f"grp_q[{r}]", gq[r, :recv[r]], o_b["grp_q"][r, :recv[r]])
+            n = int(o_b["send_off"][r, -1])
+            G.assert_eq(f"send_q[{r}]", sq[r, :n], o_b["send_q"][r, :n])
+        assert int(buf.status.item()) == 0
+
+    buf.dispatch(x, idx)             # x = A
+    x.copy_(dd_b["x"])               # a kernel writes x = B ...
+    buf.dispatch(x, idx)             # ... and the next call must see it
+    check()
+    # the same inside a graph: the copy node right before the dispatch nodes
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    x.copy_(dd_a["x"])
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=s):
+        x.copy_(dd_b["x"])
+        buf.dispatch(x, idx)
+    buf.grp_q.zero_()
+    buf.send_q.zero_()
+    x.copy_(dd_a["x"])
+    torch.cuda.synchronize()
+    g.replay()
+    check()
