@@ -36,6 +36,10 @@ struct SenderShare {
 // gives the send offsets (base); (3, sender_write) each lane adds its
 // expert's offset and its warp's prefix.  The result equals "expert offset +
 // number of earlier assignments with the same expert".
+// kOneChunk: E <= blockDim.x (the routing kernels' 1024-thread blocks), so the
+// expert scan is one block scan.  kRegRanks: single-round shares keep their
+// ranks in registers (else every rank goes through slot_row).
+template <bool kOneChunk = false, bool kRegRanks = true>
 __device__ __forceinline__ bool sender_count(int N, int T, int E, int R, int s,
                                              const int32_t *__restrict__ idx,
                                              int32_t *__restrict__ slot_row, int *smem,
@@ -62,7 +66,7 @@ __device__ __forceinline__ bool sender_count(int N, int T, int E, int R, int s,
     const int per = (TR + nw - 1) / nw;
     sh.lo = min(TR, warp * per);
     sh.hi = min(TR, sh.lo + per);
-    sh.one_round = sh.hi - sh.lo <= 32 * kAhead;
+    sh.one_round = kRegRanks && sh.hi - sh.lo <= 32 * kAhead;
     const int lo = sh.lo, hi = sh.hi;
     int *mytab = tab + warp * E;
     const unsigned lt = (1u << lane) - 1u;
@@ -101,6 +105,21 @@ __device__ __forceinline__ bool sender_count(int N, int T, int E, int R, int s,
 
     // 2. counts, prefix over warps, exclusive scan over experts (blockDim.x
     // experts at a time)
+    if constexpr (kOneChunk) {
+        int v = 0;
+        if (tid < E) {
+            for (int w = 0; w < nw; ++w) {
+                const int c = tab[w * E + tid];
+                tab[w * E + tid] = v;
+                v += c;
+            }
+        }
+        const int incl = block_inclusive_scan(v, wsum, &total);
+        if (tid < E) base[tid] = incl - v;
+        if (tid == 0) base[E] = total;
+        __syncthreads();
+        return any_bad;
+    }
     int carry = 0;
     for (int e0 = 0; e0 < E; e0 += blockDim.x) {
         const int e = e0 + tid;

@@ -17,6 +17,13 @@
 #include "launch.h"
 #include "rank.cuh"
 
+// Both routing kernels run 1024-thread blocks and the host refuses E above
+// MOE_MAX_EXPERTS (1024), so every expert owns one thread of the block and the
+// expert scan of sender_count is a single block scan (its kOneChunk form).
+#ifndef MOE_ROUTE_REG_RANKS
+#define MOE_ROUTE_REG_RANKS 1
+#endif
+
 namespace moe {
 
 constexpr int kRouteThreads = 1024;
@@ -62,7 +69,7 @@ __device__ __forceinline__ bool route_sender(int N, int T, int E, int R,
                                              int32_t *__restrict__ slot_row, int *smem) {
     int rk[kAhead];
     SenderShare sh;
-    const bool bad = sender_count(N, T, E, R, blockIdx.x, idx, slot_row, smem, rk, sh);
+    const bool bad = sender_count<true, MOE_ROUTE_REG_RANKS>(N, T, E, R, blockIdx.x, idx, slot_row, smem, rk, sh);
     sender_write(N, T, E, R, idx, cnt_out, send_off, eso_out, slot_row, smem, rk, sh, true, true);
     return bad;
 }
@@ -240,7 +247,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     if (blockIdx.x == 0 && threadIdx.x == 0) *status = 0;
     int rk[kAhead];
     SenderShare sh;
-    const bool bad = sender_count(N, T, E, R, blockIdx.x, idx, slot_row, smem, rk, sh);
+    const bool bad = sender_count<true, MOE_ROUTE_REG_RANKS>(N, T, E, R, blockIdx.x, idx, slot_row, smem, rk, sh);
     const int r = blockIdx.x, tid = threadIdx.x, Er = E / N, F = Er * N;
     const int j = tid / N, s = tid - (tid / N) * N;
     int v = 0, w = 0;
