@@ -101,13 +101,14 @@ def test_ll_output_equals_main_path():
                                        (2, 9, 32, 12, 128), (2, 5, 64, 32, 256),
                                        (2, 1024, 8, 2, 128), (4, 8, 1024, 32, 128),
                                        (3, 700, 12, 4, 256), (2, 1024, 64, 32, 128),
-                                       (5, 520, 1000, 8, 128)])
+                                       (5, 520, 1000, 8, 128), (2, 3, 4, 2, 65536)])
 def test_ll_small_shapes(N, T, E, R, H):
     """Includes more than eight slots per token (the earlier-id count runs in
     groups of eight), 32 slots, the longest batch (T = 1024) and the most
     experts (1024, the largest region-count histogram); the last three have
     more than 2048 ids per rank, so each sender's ids are ranked once in the
-    same launch (more experts than the CTA has threads in the last)."""
+    same launch (more experts than the CTA has threads in the last); the
+    widest row the ABI takes (65536 elements)."""
     w = W.Workload("llgrid", N=N, T=T, H=H, E=E, R=R, seed=N * 100 + T)
     d = W.generate(w)
     b = _run_ll(w, d, 0)
@@ -147,3 +148,48 @@ def test_ll_rejects_long_batches():
     import ctypes
     rc = m.lib().moe_dispatch_ll(ctypes.byref(sh), *([ctypes.c_void_p(p.data_ptr())] * 8), None)
     assert rc == m.MOE_ENOTSUP and z.ll_rows == 2 * 8 * 1025
+
+
+def _fill_sentinels(b):
+    b.ll_q.fill_(G.SENT_U8)
+    b.ll_s.fill_(float("nan"))
+    b.ll_src.fill_(G.SENT_I32)
+    b.ll_row.fill_(G.SENT_I32)
+    b.ll_count.fill_(G.SENT_I32)
+    b.y_ll.view(torch.int16).fill_(G.SENT_U16)
+    b.status.fill_(-1)
+
+
+@pytest.mark.parametrize("N,T,E,R,H", [(4, 32, 64, 8, 1024),     # per-token row search
+                                       (2, 1024, 16, 4, 512)])   # senders ranked first
+def test_ll_graph_replay_with_new_inputs(N, T, E, R, H):
+    """The three low-latency calls captured once in a CUDA graph and replayed
+    on two different inputs copied into the captured tensors: each replay
+    equals the oracle on its own inputs (rows, counts, payload, output), and
+    rows outside the second input's layout keep their sentinels."""
+    w = W.Workload("llgraph", N=N, T=T, H=H, E=E, R=R, seed=N * 1000 + T)
+    d_a = W.generate(w)
+    d_b = W.generate(w.replace(seed=w.seed + 1))
+    b = m.MoeLLBuffers(w.N, w.T, w.E, w.R, w.H)
+    st = G.to_dev(d_a)
+    x, idx, wt = st["x"].clone(), st["topk_idx"].clone(), st["topk_w"].clone()
+    b.dispatch(x, idx)   # load the kernels before capture
+    b.expert(1)
+    b.combine(wt)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        b.dispatch(x, idx)
+        b.expert(1)
+        b.combine(wt)
+    for d in (d_a, d_b):
+        dd = G.to_dev(d)
+        x.copy_(dd["x"])
+        idx.copy_(dd["topk_idx"])
+        wt.copy_(dd["topk_w"])
+        _fill_sentinels(b)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        _check_ll(w, d, b, 1)

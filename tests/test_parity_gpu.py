@@ -343,12 +343,13 @@ def test_many_experts_per_token(N, T, E, R, H, calls):
 
 
 @pytest.mark.parametrize("N,T,E,R,H", [(4, 8, 1024, 32, 128), (64, 4, 128, 2, 256),
-                                       (1, 1024, 16, 4, 128)])
+                                       (1, 1024, 16, 4, 128), (2, 3, 4, 2, 65536)])
 @pytest.mark.parametrize("calls", ["fused", "separate", "signalled"])
 def test_limits(N, T, E, R, H, calls):
     """At the ABI's limits: the most experts (1024, the route's largest
     shared-memory tables) with the most slots (32), 64 ranks (the route
-    without a cluster, many blocks), and one rank with the longest batch."""
+    without a cluster, many blocks), one rank with the longest batch, and
+    the widest row (65536 elements: many pieces per row, 512 scales)."""
     w = W.Workload("limits", N=N, T=T, H=H, E=E, R=R, seed=2000 + N + E)
     d = W.generate(w)
     G.compare_with_oracle(w, G.run_path(w, G.to_dev(d), calls=calls),
