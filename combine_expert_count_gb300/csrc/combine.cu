@@ -29,7 +29,22 @@ constexpr int kReduceGroup = 8;  // row loads kept in flight per chunk
 // measured 84.6 us against 86.7 us with whole tokens (finer work evens out
 // the last wave of blocks); 4 or 8 were no better; on H = 2048 rows the
 // split would leave half of every block idle.
-static int combine_split(int H) { return (H >> 3) >= 2 * kGatherThreads ? 2 : 1; }
+static int combine_split(int H, int threads) { return (H >> 3) >= 2 * threads ? 2 : 1; }
+
+// Threads per block of the fused combine: kGatherThreads, or half as many
+// for rows of at most MOE_GATHER_NARROW_H elements, so that a short row
+// (2048 elements: 256 16-byte chunks) is still split over two blocks, each
+// thread one chunk of every row.  On the Qwen3-shaped EP16 combine
+// (H = 2048) that measured 94.5 against 98.1 us and the layer graph 153.2
+// against 156.5 us; on 7168-element rows 128 threads were slower (Kimi-K2
+// EP32 layer 261 against 257 us).
+#ifndef MOE_GATHER_NARROW_H
+#define MOE_GATHER_NARROW_H 2048
+#endif
+constexpr int kGatherNarrow = kGatherThreads / 2;
+static int gather_threads(int H) {
+    return H <= MOE_GATHER_NARROW_H && kGatherNarrow >= 32 ? kGatherNarrow : kGatherThreads;
+}
 
 // kLL: the rows come from the low-latency layout, row ll_row[s][t][k] of
 // `csend` (there y_ll), instead of the combine send buffers.
@@ -159,8 +174,10 @@ cudaError_t launch_combine_ll(const moe_shape &sh, const uint16_t *y_ll, const f
 // folds the same values into the fp32 accumulator in slot order, as
 // moe_combine_recv would after reading them back.  A row whose grouped
 // position was dropped is written as zeros and contributes w * 0.
-template <int KR>  // 0: slots read from shared memory; else R <= KR slots held in registers
-__global__ void __launch_bounds__(kGatherThreads)
+// KR: 0, slots read from shared memory; else R <= KR slots held in registers.
+// kThreads: the block size it is launched with.
+template <int KR, int kThreads>
+__global__ void __launch_bounds__(kThreads)
     k_combine_fused(int N, int T, int E, int R, int H, int cap, int split,
                     const uint16_t *__restrict__ y,
                     const int32_t *__restrict__ idx, const float *__restrict__ w,
@@ -272,21 +289,23 @@ cudaError_t launch_combine_fused(const moe_shape &sh, int cap, const uint16_t *y
     const long long ntok = (long long)sh.N * sh.T;
     if (ntok <= 0) return cudaSuccess;
     const int kr = sh.R <= 8 ? 8 : 0;
-    auto kern = kr ? k_combine_fused<8> : k_combine_fused<0>;
+    const int threads = gather_threads(sh.H);
+    const bool narrow = threads != kGatherThreads;
+    auto kern = kr ? (narrow ? k_combine_fused<8, kGatherNarrow> : k_combine_fused<8, kGatherThreads>)
+                   : (narrow ? k_combine_fused<0, kGatherNarrow> : k_combine_fused<0, kGatherThreads>);
     static LaunchMemo memo;
     int occ = 1;
-    const cudaError_t err = memo.get(kr, &occ, [&](int *v) {
-        const cudaError_t e =
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(v, kern, kGatherThreads, 0);
+    const cudaError_t err = memo.get(kr * 2 + (narrow ? 1 : 0), &occ, [&](int *v) {
+        const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(v, kern, threads, 0);
         if (*v < 1) *v = 1;
         return e;
     });
     if (err != cudaSuccess) return err;
     // small batches: more blocks per token, as for the reduce
-    const int split = token_split(ntok, sh.H, kGatherThreads, occ, combine_split(sh.H));
+    const int split = token_split(ntok, sh.H, threads, occ, combine_split(sh.H, threads));
     const long long nblk = ntok * split;
     const int grid = (int)(nblk < (1LL << 30) ? nblk : (1LL << 30));
-    return launch_kernel(kern, dim3((unsigned)grid), dim3(kGatherThreads), 0, st, sh.N, sh.T, sh.E,
+    return launch_kernel(kern, dim3((unsigned)grid), dim3(threads), 0, st, sh.N, sh.T, sh.E,
                          sh.R, sh.H, cap, split, y, idx, w, slot_row, eso, seg_off, send_off,
                          csend_off, csend, out);
 }
