@@ -25,14 +25,17 @@ __device__ __forceinline__ uint32_t cvt_pair(float a, float b) {
 // One CTA works through (token, piece) items, a piece being up to
 // kPieceElems elements of the row (a multiple of 128, so no scale block
 // straddles two pieces).  Per item: the bf16 piece arrives in shared memory
-// by one bulk copy (issued one item ahead, completion on an mbarrier); the
+// by one bulk copy (issued into a ring of x buffers up to kNB - 1 items
+// ahead, completion on the buffer's mbarrier); the
 // threads quantise it, 16 elements per thread and 8 threads per 128-element
 // block (amax by xor-shuffles within the group, scale = amax/448 and
 // q = e4m3_satfinite_rn(x/scale) with IEEE fp32 divisions), and each thread
 // stores its 16 fp8 bytes straight from registers to the same place in each
 // of the token's R destination rows (one 512-byte coalesced store per warp
-// and row), the group's first thread also the scale.  Two x buffers let the
-// load of item n+1 overlap the arithmetic and stores of item n.  The fused
+// and row), the group's first thread also the scale.  The ring (four
+// buffers for the send and fused forms, two for the others: x_stages) lets
+// the loads of the next items overlap the arithmetic and stores of item n.
+// The fused
 // and low-latency forms store their fp8 rows evict-first (st.global.cs):
 // nothing in the layer reads them again, and the DSv3 EP16 layer (dispatch,
 // then combine, as one graph) took 137.6 us against 138.8 with default
