@@ -23,6 +23,18 @@ namespace moe {
 
 static_assert(kReduceThreads >= 32 && kGatherThreads >= 32, "warp 0 sorts the slots");
 
+// The sending side and the one-pass form take the fused combine's block
+// shape: half of kGatherThreads for rows of at most MOE_GATHER_NARROW_H
+// elements, and two blocks per token when half of every row still gives
+// each thread a 16-byte chunk.  Against 256 threads and one block per
+// token: the Qwen3-shaped EP16 one-pass form 93.4 against 95.8 us (layer
+// graph 151.1 against 153.1), DSv3 EP16 79.4 against 81.5 (layer 130.8
+// against 132.7), Kimi-K2 unchanged.
+#ifndef MOE_GATHER_NARROW_H
+#define MOE_GATHER_NARROW_H 2048
+#endif
+static_assert(kGatherThreads / 2 >= 32, "the narrow block still holds warp 0's sort");
+
 enum class PartialMode { kSend, kRecv, kFused };
 
 template <PartialMode kMode, int KR>  // KR > 0: R <= KR rows in registers; 0: any R
@@ -173,16 +185,20 @@ static cudaError_t launch_partial(const moe_shape &sh, int cap, const uint16_t *
     const int kr = sh.R <= 8 ? 8 : 0;
     auto kern = kr ? k_combine_partial<kMode, 8> : k_combine_partial<kMode, 0>;
     // the receiving side only reads rows: the smaller block (see bf16.cuh)
-    const int threads = kMode == PartialMode::kRecv ? kReduceThreads : kGatherThreads;
+    int threads = kReduceThreads, least = 1;
+    if (kMode != PartialMode::kRecv) {
+        threads = sh.H <= MOE_GATHER_NARROW_H ? kGatherThreads / 2 : kGatherThreads;
+        least = (sh.H >> 3) >= 2 * threads ? 2 : 1;
+    }
     static LaunchMemo memo;
     int occ = 1;
-    const cudaError_t err = memo.get(kr, &occ, [&](int *v) {
+    const cudaError_t err = memo.get(kr * 1024 + threads, &occ, [&](int *v) {
         const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(v, kern, threads, 0);
         if (*v < 1) *v = 1;
         return e;
     });
     if (err != cudaSuccess) return err;
-    const int split = token_split(ntok, sh.H, threads, occ, 1);
+    const int split = token_split(ntok, sh.H, threads, occ, least);
     const long long nblk = ntok * split;
     const int grid = (int)(nblk < (1LL << 30) ? nblk : (1LL << 30));
     return launch_kernel(kern, dim3((unsigned)grid), dim3(threads), 0, st, sh.N, sh.T,
