@@ -242,6 +242,15 @@ __device__ __forceinline__ int quant_pack_body(
     }
     __syncthreads();
 
+    // host x: the threads copy the piece with 16-byte loads
+    auto host_copy = [&](long long item, int b) {
+        const long long tok = tok0 + div_nonneg(item, npieces);
+        const int off = (int)(item - div_nonneg(item, npieces) * npieces) * P;
+        const int len = min(P, H - off);
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + tok * H + off);
+        uint4 *dst = reinterpret_cast<uint4 *>(xbuf + (size_t)b * P);
+        for (int i = threadIdx.x; i < (len >> 3); i += blockDim.x) dst[i] = src[i];
+    };
     auto issue_load = [&](long long item, int b) {
         const long long tok = tok0 + div_nonneg(item, npieces);
         const int off = (int)(item - div_nonneg(item, npieces) * npieces) * P;
@@ -257,6 +266,13 @@ __device__ __forceinline__ int quant_pack_body(
     if (!kHostX && tid == 0)
         for (int i = 0; i < kPre && first + (long long)i * G < nitems; ++i)
             issue_load(first + (long long)i * G, i);
+    if constexpr (kHostX && Gate::kPrefetch) {
+        // host x is no output of the kernel before the gate either: every
+        // buffer's piece crosses the link while that kernel runs
+        for (int i = 0; i < kXStages && first + (long long)i * G < nitems; ++i)
+            host_copy(first + (long long)i * G, i);
+        __syncthreads();
+    }
     if constexpr (Gate::kPrefetch) gate(reinterpret_cast<int *>(sm + stage_bytes(P, kXStages)));
     bool timed_out = false;
     // thread tid < R: destinations of the current item, read one item ahead
@@ -347,9 +363,7 @@ __device__ __forceinline__ int quant_pack_body(
             grows[tid] = pgrow;
         }
         if constexpr (kHostX) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(x + tok * H + off);
-            uint4 *dst = reinterpret_cast<uint4 *>(xbuf + (size_t)b * P);
-            for (int i = tid; i < (len >> 3); i += nthr) dst[i] = src[i];
+            if (!(Gate::kPrefetch && n < kXStages)) host_copy(item, b);
             __syncthreads();
         } else {
             const bool ok = mbar_wait(&xbar[b], par);

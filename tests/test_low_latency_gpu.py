@@ -193,3 +193,29 @@ def test_ll_graph_replay_with_new_inputs(N, T, E, R, H):
         g.replay()
         torch.cuda.synchronize()
         _check_ll(w, d, b, 1)
+
+
+@pytest.mark.parametrize("N,T,E,R,H", [(16, 32, 256, 8, 7168),   # per-token row search
+                                       (2, 1024, 16, 4, 512)])   # senders ranked first
+def test_ll_pinned_host_x(N, T, E, R, H):
+    """x read from pinned host memory by the low-latency dispatch gives the
+    same rows, counts and output as x in device memory."""
+    w = W.Workload("llhost", N=N, T=T, H=H, E=E, R=R, seed=N * 10 + T)
+    d = W.generate(w)
+    ref_b = _run_ll(w, d, 1)
+    dd = G.to_dev(d)
+    b = m.MoeLLBuffers(w.N, w.T, w.E, w.R, w.H)
+    _fill_sentinels(b)
+    xh = torch.empty(dd["x"].shape, dtype=dd["x"].dtype, pin_memory=True)
+    xh.copy_(dd["x"])
+    b.dispatch(xh, dd["topk_idx"])
+    b.expert(1)
+    b.combine(dd["topk_w"])
+    torch.cuda.synchronize()
+    for k in ("ll_row", "ll_count", "status", "out"):
+        assert torch.equal(getattr(b, k).view(torch.uint8), getattr(ref_b, k).view(torch.uint8)), k
+    rows = ref_b.ll_row.flatten()
+    rows = rows[rows >= 0].long()
+    for k in ("ll_q", "ll_s", "ll_src"):
+        assert torch.equal(getattr(b, k)[rows].view(torch.uint8),
+                           getattr(ref_b, k)[rows].view(torch.uint8)), k
