@@ -13,6 +13,26 @@ namespace moe {
 // waits on one memory round trip per kAhead rounds, not per round.
 constexpr int kAhead = 8;
 
+// The lanes whose key equals this lane's, over the full warp (what
+// __match_any_sync returns), for keys in [0, 2^nbits): one ballot per key
+// bit, each lane keeping the lanes that agree with it on every bit.
+#ifndef MOE_BALLOT_PEERS
+#define MOE_BALLOT_PEERS 1
+#endif
+__device__ __forceinline__ unsigned warp_peers(int key, int nbits) {
+    if (!MOE_BALLOT_PEERS) return __match_any_sync(kFull, key);
+    unsigned peers = kFull;
+    for (int b = 0; b < nbits; ++b) {
+        const bool bit = (key >> b) & 1;
+        const unsigned m = __ballot_sync(kFull, bit);
+        peers &= bit ? m : ~m;
+    }
+    return peers;
+}
+
+// Bits of the ranking keys: experts 0..E-1, and E for an id outside [0, E).
+__device__ __forceinline__ int key_bits(int E) { return 32 - __clz(E); }
+
 // Where a sender's warp keeps the ranks of its share between the passes:
 // in registers when the share is one load round (rk), else in slot_row.
 struct SenderShare {
@@ -27,7 +47,7 @@ struct SenderShare {
 //
 // Stable slots in three passes, whatever T*R is: (1) warp w walks its own
 // contiguous share of the rank's ids, 32 at a time; lanes holding the same
-// expert find each other with __match_any_sync, the group's first lane adds
+// expert find each other (warp_peers), the group's first lane adds
 // the group to the warp's running count of that expert (a table row of its
 // own, so no block barrier is needed) and every lane keeps "running count
 // before its group + its rank in the group" -- its rank among equal ids in
@@ -70,6 +90,7 @@ __device__ __forceinline__ bool sender_count(int N, int T, int E, int R, int s,
     const int lo = sh.lo, hi = sh.hi;
     int *mytab = tab + warp * E;
     const unsigned lt = (1u << lane) - 1u;
+    const int nbits = key_bits(E);
     int bad = 0;
     for (int r0 = lo; r0 < hi; r0 += 32 * kAhead) {
         int ev[kAhead];
@@ -85,7 +106,7 @@ __device__ __forceinline__ bool sender_count(int N, int T, int E, int R, int s,
             const int e = ev[u];
             const bool good = (unsigned)e < (unsigned)E;
             if (i < hi && !good) bad = 1;
-            const unsigned peers = __match_any_sync(kFull, good ? e : -1);
+            const unsigned peers = warp_peers(good ? e : E, nbits);
             const int leader = __ffs(peers) - 1;
             int before = 0;
             if (good && lane == leader) {

@@ -346,13 +346,18 @@ def test_many_experts_per_token(N, T, E, R, H, calls):
 
 
 @pytest.mark.parametrize("N,T,E,R,H", [(4, 8, 1024, 32, 128), (64, 4, 128, 2, 256),
-                                       (1, 1024, 16, 4, 128), (2, 3, 4, 2, 65536)])
+                                       (1, 1024, 16, 4, 128), (2, 3, 4, 2, 65536),
+                                       (20, 256, 40, 8, 128), (16, 300, 32, 8, 128),
+                                       (32, 128, 32, 8, 128)])
 @pytest.mark.parametrize("calls", ["fused", "separate", "signalled"])
 def test_limits(N, T, E, R, H, calls):
     """At the ABI's limits: the most experts (1024, the route's largest
     shared-memory tables) with the most slots (32), 64 ranks (the route
-    without a cluster, many blocks), one rank with the longest batch, and
-    the widest row (65536 elements: many pieces per row, 512 scales)."""
+    without a cluster, many blocks), one rank with the longest batch, the
+    widest row (65536 elements: many pieces per row, 512 scales); and the
+    routing kernel's forms with many ids per rank: 20 and 32 ranks (the
+    grid-barrier route) and 16 ranks with 2400 ids each (the cluster
+    route)."""
     w = W.Workload("limits", N=N, T=T, H=H, E=E, R=R, seed=2000 + N + E)
     d = W.generate(w)
     G.compare_with_oracle(w, G.run_path(w, G.to_dev(d), calls=calls),
