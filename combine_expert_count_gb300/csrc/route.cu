@@ -106,7 +106,8 @@ __device__ __forceinline__ void route_receiver(int N, int E, int cap, int v, int
     const int recv = total;
     if (tid == 0) excl[F] = recv;
     __syncthreads();
-    if (tid <= Er) grp_off[(size_t)r * (Er + 1) + tid] = excl[tid * N];
+    // Er + 1 entries: one more than the block's threads when Er = blockDim.x
+    for (int j = tid; j <= Er; j += blockDim.x) grp_off[(size_t)r * (Er + 1) + j] = excl[j * N];
     if (tid < Er) m_sizes[(size_t)r * Er + tid] = excl[(tid + 1) * N] - excl[tid * N];
     if (tid == 0 && recv > cap) flag(status, MOE_ST_CAPACITY);
     const int wi = block_inclusive_scan(w, wsum, &total);

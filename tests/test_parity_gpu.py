@@ -234,6 +234,27 @@ def test_bad_expert_ids_are_skipped_and_flagged(calls):
     assert G.host(buf.slot_row)[0, 1, 1] == -1
 
 
+@pytest.mark.parametrize("E", [1, 7, 8, 64, 255, 256, 1023, 1024])
+@pytest.mark.parametrize("calls", ["fused", "separate"])
+def test_ranking_keys_at_bit_boundaries(E, calls):
+    """The routing kernels find equal ids with one warp ballot per bit of a
+    key (expert id, or E for an id outside [0, E)): expert counts just below
+    and at a power of two, bad ids of every kind, and whole warps of one
+    expert give the oracle's counts, slots and layouts."""
+    R = min(3, E)
+    w = W.Workload("keys", N=1, T=96, H=128, E=E, R=R, seed=E)
+    d = W.generate(w)
+    ids = d["topk_idx"]
+    ids[0, 0:11, 0] = E - 1              # a run of the highest expert
+    ids[0, 40:72, :] = 0                 # whole warps of expert 0 (repeated slots)
+    for t, v in ((3, -1), (17, E), (29, E + 1), (50, 2 * E), (77, 1 << 30), (90, -(1 << 30))):
+        ids[0, t, R - 1] = v
+    o = _oracle(w, d, w.N * w.T * w.R)
+    assert o["status"] == ref.ST_BAD_EXPERT
+    buf = G.run_path(w, G.to_dev(d), cap=w.N * w.T * w.R, calls=calls)
+    G.compare_with_oracle(w, buf, o)
+
+
 @pytest.mark.parametrize("cap", [1, 7, 20])
 @pytest.mark.parametrize("calls", ["fused", "separate", "fused_route"])
 def test_capacity_overflow_drops_and_flags(cap, calls):
@@ -348,7 +369,7 @@ def test_many_experts_per_token(N, T, E, R, H, calls):
 @pytest.mark.parametrize("N,T,E,R,H", [(4, 8, 1024, 32, 128), (64, 4, 128, 2, 256),
                                        (1, 1024, 16, 4, 128), (2, 3, 4, 2, 65536),
                                        (20, 256, 40, 8, 128), (16, 300, 32, 8, 128),
-                                       (32, 128, 32, 8, 128)])
+                                       (32, 128, 32, 8, 128), (1, 64, 1024, 32, 128)])
 @pytest.mark.parametrize("calls", ["fused", "separate", "signalled"])
 def test_limits(N, T, E, R, H, calls):
     """At the ABI's limits: the most experts (1024, the route's largest
@@ -357,7 +378,8 @@ def test_limits(N, T, E, R, H, calls):
     widest row (65536 elements: many pieces per row, 512 scales); and the
     routing kernel's forms with many ids per rank: 20 and 32 ranks (the
     grid-barrier route) and 16 ranks with 2400 ids each (the cluster
-    route)."""
+    route); one rank holding all 1024 experts with 32 slots (as many local
+    experts as the routing block has threads)."""
     w = W.Workload("limits", N=N, T=T, H=H, E=E, R=R, seed=2000 + N + E)
     d = W.generate(w)
     G.compare_with_oracle(w, G.run_path(w, G.to_dev(d), calls=calls),
