@@ -101,14 +101,16 @@ def test_ll_output_equals_main_path():
                                        (2, 9, 32, 12, 128), (2, 5, 64, 32, 256),
                                        (2, 1024, 8, 2, 128), (4, 8, 1024, 32, 128),
                                        (3, 700, 12, 4, 256), (2, 1024, 64, 32, 128),
-                                       (5, 520, 1000, 8, 128), (2, 3, 4, 2, 65536)])
+                                       (5, 520, 1000, 8, 128), (2, 3, 4, 2, 65536),
+                                       (1, 16, 1024, 32, 128), (1, 1024, 64, 4, 128)])
 def test_ll_small_shapes(N, T, E, R, H):
     """Includes more than eight slots per token (the earlier-id count runs in
     groups of eight), 32 slots, the longest batch (T = 1024) and the most
     experts (1024, the largest region-count histogram); the last three have
     more than 2048 ids per rank, so each sender's ids are ranked once in the
     same launch (more experts than the CTA has threads in the last); the
-    widest row the ABI takes (65536 elements)."""
+    widest row the ABI takes (65536 elements); one rank holding all 1024
+    experts, and one rank ranking 4096 ids."""
     w = W.Workload("llgrid", N=N, T=T, H=H, E=E, R=R, seed=N * 100 + T)
     d = W.generate(w)
     b = _run_ll(w, d, 0)

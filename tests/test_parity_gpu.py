@@ -354,7 +354,7 @@ def test_e4m3_encoder_matches_oracle_exhaustively():
 
 
 @pytest.mark.parametrize("N,T,E,R,H", [(2, 9, 32, 12, 128), (2, 5, 64, 32, 256),
-                                       (3, 4, 24, 9, 384)])
+                                       (3, 4, 24, 9, 384), (4, 6, 32, 32, 256)])
 @pytest.mark.parametrize("calls", ["fused", "separate", "fused_route", "signalled"])
 def test_many_experts_per_token(N, T, E, R, H, calls):
     """More than eight slots per token (the quantiser stores to every slot's
