@@ -761,7 +761,10 @@ cudaError_t launch_dispatch_ll(const moe_shape &sh, const uint16_t *x, const int
     ll.idx = idx;
     ll.ll_row = ll_row;
     ll.ll_count = ll_count;
-    if ((long long)sh.N * sh.T <= 0) return cudaSuccess;
+    // an empty batch: every region is empty (the kernels write the counts
+    // from each sender's token 0, and there is none)
+    if ((long long)sh.N * sh.T <= 0)
+        return cudaMemsetAsync(ll_count, 0, (size_t)sh.N * sh.E * sizeof(int32_t), st);
     if ((long long)sh.T * sh.R > MOE_LL_SEARCH_MAX) {
         if (is_host_memory(x))
             return launch_ll_ranked_x<true>(sh, x, ll_q, ll_s, ll_src, status, ll, st);

@@ -415,8 +415,8 @@ int moe_dispatch_signalled_static(const moe_shape *shape, const moe_buffers *b, 
  * 1024 (MOE_ENOTSUP beyond), N*E*T < 2^31. */
 
 /* Quantise every token (as moe_dispatch_send) and place its rows, scales and
- * token id in the low-latency layout; writes ll_row and ll_count.  Clears
- * *status first; MOE_ST_BAD_EXPERT / MOE_ST_CAPACITY as for the main path.
+ * token id in the low-latency layout; writes ll_row and ll_count (all zero
+ * for an empty batch).  Clears *status first; MOE_ST_BAD_EXPERT / MOE_ST_CAPACITY as for the main path.
  * One kernel: with at most 2048 ids per rank each token's rows come from a
  * count of the sender's earlier ids; longer batches rank every sender's ids
  * once in the same (co-resident) launch first.  The outputs are the same. */

@@ -221,3 +221,21 @@ def test_ll_pinned_host_x(N, T, E, R, H):
     for k in ("ll_q", "ll_s", "ll_src"):
         assert torch.equal(getattr(b, k)[rows].view(torch.uint8),
                            getattr(ref_b, k)[rows].view(torch.uint8)), k
+
+
+def test_ll_empty_batch():
+    """No tokens: every region count is zero, the status clear, and the
+    stand-in and combine have nothing to do."""
+    w = W.Workload("llempty", N=4, T=0, H=256, E=8, R=2)
+    b = m.MoeLLBuffers(w.N, w.T, w.E, w.R, w.H)
+    b.ll_count.fill_(G.SENT_I32)
+    b.status.fill_(-1)
+    x = torch.zeros(16, dtype=torch.int16, device="cuda")
+    idx = torch.zeros(16, dtype=torch.int32, device="cuda")
+    wt = torch.zeros(16, dtype=torch.float32, device="cuda")
+    b.dispatch(x, idx)
+    b.expert(1)
+    b.combine(wt)
+    torch.cuda.synchronize()
+    assert int(b.status.item()) == 0
+    assert torch.all(b.ll_count == 0)
