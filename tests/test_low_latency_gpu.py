@@ -102,7 +102,8 @@ def test_ll_output_equals_main_path():
                                        (2, 1024, 8, 2, 128), (4, 8, 1024, 32, 128),
                                        (3, 700, 12, 4, 256), (2, 1024, 64, 32, 128),
                                        (5, 520, 1000, 8, 128), (2, 3, 4, 2, 65536),
-                                       (1, 16, 1024, 32, 128), (1, 1024, 64, 4, 128)])
+                                       (1, 16, 1024, 32, 128), (1, 1024, 64, 4, 128),
+                                       (32, 1, 1024, 32, 128)])
 def test_ll_small_shapes(N, T, E, R, H):
     """Includes more than eight slots per token (the earlier-id count runs in
     groups of eight), 32 slots, the longest batch (T = 1024) and the most

@@ -369,7 +369,8 @@ def test_many_experts_per_token(N, T, E, R, H, calls):
 @pytest.mark.parametrize("N,T,E,R,H", [(4, 8, 1024, 32, 128), (64, 4, 128, 2, 256),
                                        (1, 1024, 16, 4, 128), (2, 3, 4, 2, 65536),
                                        (20, 256, 40, 8, 128), (16, 300, 32, 8, 128),
-                                       (32, 128, 32, 8, 128), (1, 64, 1024, 32, 128)])
+                                       (32, 128, 32, 8, 128), (1, 64, 1024, 32, 128),
+                                       (32, 1, 1024, 32, 128)])
 @pytest.mark.parametrize("calls", ["fused", "separate", "signalled"])
 def test_limits(N, T, E, R, H, calls):
     """At the ABI's limits: the most experts (1024, the route's largest
@@ -379,7 +380,8 @@ def test_limits(N, T, E, R, H, calls):
     routing kernel's forms with many ids per rank: 20 and 32 ranks (the
     grid-barrier route) and 16 ranks with 2400 ids each (the cluster
     route); one rank holding all 1024 experts with 32 slots (as many local
-    experts as the routing block has threads)."""
+    experts as the routing block has threads); one token per rank on 32
+    ranks with 1024 experts and 32 slots."""
     w = W.Workload("limits", N=N, T=T, H=H, E=E, R=R, seed=2000 + N + E)
     d = W.generate(w)
     G.compare_with_oracle(w, G.run_path(w, G.to_dev(d), calls=calls),

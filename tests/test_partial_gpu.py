@@ -61,11 +61,13 @@ def test_config_parity(name, calls):
 @pytest.mark.parametrize("N,T,E,R,H", [(1, 3, 2, 2, 128), (2, 5, 8, 3, 256), (4, 16, 16, 4, 384),
                                        (3, 7, 12, 8, 128), (4, 4, 32, 12, 256),
                                        (2, 9, 64, 32, 128), (4, 8, 1024, 32, 128),
-                                       (1, 16, 1024, 32, 128), (2, 40, 8, 8, 2048)])
+                                       (1, 16, 1024, 32, 128), (2, 40, 8, 8, 2048),
+                                       (2, 3, 4, 2, 65536), (32, 1, 1024, 32, 128)])
 def test_small_shapes_and_many_experts(N, T, E, R, H):
     """Includes R > 8 (the shared-memory slot loop), R = 32, one rank
-    holding all 1024 experts, and 2048-element rows (the narrow blocks, two
-    per token) with every expert of a rank taken by each token."""
+    holding all 1024 experts, 2048-element rows (the narrow blocks, two per
+    token) with every expert of a rank taken by each token, the widest row,
+    and one token per rank on 32 ranks with 1024 experts and 32 slots."""
     w = W.Workload("grid", N=N, T=T, H=H, E=E, R=R, seed=41 + N * 100 + T * 10 + R)
     d = W.generate(w)
     for calls in ("partial", "partial_separate"):
