@@ -65,6 +65,22 @@ def test_static_scratch_matches_caller_scratch_two_calls(name, T):
             assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), (name_, seed)
 
 
+def test_static_scratch_at_its_limit():
+    """64 ranks, the most the static scratch holds: the same outputs as the
+    caller's scratch."""
+    w = W.Workload("static64", N=64, T=4, H=256, E=128, R=2, seed=64)
+    want, got = _bufs(w), _bufs(w)
+    sig = torch.zeros(int(want.sizes.bytes_sig) // 4, dtype=torch.int32, device="cuda")
+    x, idx = _inputs(w, 303)
+    m.moe_dispatch_signalled(want.shape, want.tensors(x=x, topk_idx=idx), sig)
+    m.moe_dispatch_signalled_static(got.shape, got.tensors(x=x, topk_idx=idx))
+    torch.cuda.synchronize()
+    assert int(want.status.item()) == 0 and int(got.status.item()) == 0
+    for name_ in OUTPUTS:
+        a, b = getattr(want, name_), getattr(got, name_)
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), name_
+
+
 def test_beyond_the_static_limit_is_rejected():
     sh = m.make_shape(128, 4, 128, 2, 256)
     z = m.sizes_query(sh)
