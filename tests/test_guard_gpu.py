@@ -54,7 +54,9 @@ def _inputs(w):
 
 
 @pytest.mark.parametrize("N,T,E,R,H", [(2, 16, 8, 2, 256), (3, 5, 12, 9, 640),
-                                       (2, 3, 4, 2, 8192 + 1024), (4, 7, 32, 32, 128)])
+                                       (2, 3, 4, 2, 8192 + 1024), (4, 7, 32, 32, 128),
+                                       (1, 64, 1024, 32, 128), (2, 40, 8, 8, 2048),
+                                       (2, 600, 8, 4, 256), (2, 3, 4, 2, 65536)])
 def test_no_write_past_any_buffer(N, T, E, R, H):
     w = W.Workload("guard", N=N, T=T, H=H, E=E, R=R, seed=71)
     x, idx, wt = _inputs(w)
