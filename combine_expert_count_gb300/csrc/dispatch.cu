@@ -37,9 +37,13 @@ __device__ __forceinline__ uint32_t cvt_pair(float a, float b) {
 // the loads of the next items overlap the arithmetic and stores of item n.
 // The fused
 // and low-latency forms store their fp8 rows evict-first (st.global.cs):
-// nothing in the layer reads them again, and the DSv3 EP16 layer (dispatch,
-// then combine, as one graph) took 137.6 us against 138.8 with default
-// stores, the dispatch itself unchanged.  The send-only form keeps default
+// nothing in the dispatch + combine step reads them again (the send rows are
+// the wire copy; the grouped rows are read by the grouped GEMM, which runs
+// between the two halves and outside this library), and the DSv3 EP16 layer
+// (dispatch, then combine, as one graph) took 137.6 us against 138.8 with
+// default stores, the dispatch itself unchanged.  A caller whose GEMM runs
+// right after the dispatch and could find the grouped rows in L2 gives up
+// that chance with these stores.  The send-only form keeps default
 // stores: its rows are read back next (by the receive pull, or by the
 // signalled kernel's own copy phase), which evict-first stores made 4 and
 // 1.2 us slower.
