@@ -346,6 +346,20 @@ def oracle_all_cores(w, d, steps: int = 2, procs: int = 0) -> dict:
                    "wall time / layers"}
 
 
+def cpu_model() -> str:
+    """The host CPU's model name as lscpu reports it (on Arm it decodes the
+    part number), else the architecture."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.startswith("Model name:"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.processor() or platform.machine()
+
+
 def cpu_baseline_line(w, d, min_seconds: float, all_cores: bool, warmup: int = 1,
                       max_reps: int = 1000) -> dict:
     import platform
@@ -357,7 +371,7 @@ def cpu_baseline_line(w, d, min_seconds: float, all_cores: bool, warmup: int = 1
                       "combine_send + combine_recv, stand-in outside the timer",
             "dispatch_us": round(dus, 1), "combine_us": round(cus, 1),
             "layers": reps, "cpu_seconds": round(spent, 2),
-            "cpu": platform.processor() or platform.machine(), "nproc": os.cpu_count()}
+            "cpu": cpu_model(), "arch": platform.machine(), "nproc": os.cpu_count()}
     if all_cores:
         line["all_cores"] = oracle_all_cores(w, d)
     return line
@@ -536,7 +550,7 @@ def oracle_table(args) -> None:
     from combine_expert_count_gb300 import workloads as W
     from oracle import ref
     ref.build()
-    out = {"cpu": platform.processor() or platform.machine(), "nproc": os.cpu_count(),
+    out = {"cpu": cpu_model(), "arch": platform.machine(), "nproc": os.cpu_count(),
            "configs": []}
     for name in ("tiny", "dsv3_decode", "kimi_k2_decode", "qwen3_skew", "qwen3_worst", "prefill"):
         w = W.CONFIGS[name]
